@@ -1,0 +1,210 @@
+/*
+ * vg.h — C ABI of the Vegas hot path on one GB300 (sm_103a).
+ *
+ * Verification-guided sparse self-speculative decoding, as described on the page
+ * "Resumo Técnico: Vegas – Decodificação Auto-Especulativa com Atenção Esparsa
+ * Guiada por Verificação" (gist.science summary of paper 2602.07223), cited below
+ * as "Vegas §<section>".  One iteration has three device steps:
+ *
+ *   vg_verify_attn        full attention of the gamma+1 verify rows over the KV cache
+ *                         (Vegas §2 step 1), which also sums the pre-softmax logits of
+ *                         every prefix entry over the chosen rows and all query heads
+ *                         (Vegas §2.A formula, §2.B Collect-2-Query, §3 instrumentation);
+ *   vg_topk_select        the k prefix entries with the largest summed logit
+ *                         (Vegas §2 step 2, the argmax of §2.A);
+ *   vg_sparse_draft_attn  one draft step's attention over the selected entries plus the
+ *                         draft tokens appended so far, gathered token by token
+ *                         (Vegas §2 step 3; §3 sparse execution, page size one).
+ *   vg_iteration          verify -> select -> gamma draft steps, in stream order.
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are DEVICE pointers to caller-owned memory, unless a
+ *     comment says "host".  The library never allocates, frees or synchronises,
+ *     and never keeps a pointer after a call returns.
+ *   - bf16 is IEEE bfloat16 (uint16 storage); fp32 is IEEE binary32.
+ *   - Every call only enqueues work on `stream` (0 = legacy default stream) and
+ *     returns.  Arguments are validated on the host before anything is enqueued;
+ *     a call that returns an error has enqueued nothing.
+ *   - Device-side checks (a prefix length above max_len, an index outside the
+ *     allowed range, a bounded wait that ran out) never fault: the kernel skips the
+ *     offending item and writes a VG_ERR_* code into *dev_status (if dev_status is
+ *     non-NULL; the first error wins, the caller zeroes it).  Results for a sequence
+ *     whose inputs failed a device check are unspecified.
+ *   - Alignment: every device pointer must be 16-byte aligned (dev_status: 4-byte).
+ *   - Workspace: `ws` is caller-owned device scratch of at least
+ *     vg_workspace_size(...) bytes, 256-byte aligned.  Its contents need no
+ *     initialisation and are garbage after a call.  Calls that share a workspace
+ *     must be ordered on one stream.
+ *   - Thread safety: calls may be made from several host threads; vg_last_error()
+ *     is per thread.
+ *
+ * KV cache (Vegas §1: one K and one V entry per token, growing with the context)
+ *   Token-granular slot pool: K and V are bf16 [capacity_slots][H_kv][d], one slot
+ *   per token holding all KV heads contiguously (the "page size of one token" of
+ *   Vegas §3).  Sequence b's token i lives in slot seq_offset[b] + i.  The caller
+ *   reserves, after each prefix, room for the gamma+1 verify rows.
+ *
+ * Shapes supported by this build: d in {64, 128}; H_kv in [1, 16]; H_q = G * H_kv
+ * with G in [1, 16]; gamma in [0, 15]; G * (gamma+1) <= 64; 1 <= B <= 1024;
+ * max_len <= 262144 for vg_topk_select; k >= 1.
+ */
+#ifndef VG_H
+#define VG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t vg_status;
+
+#define VG_OK 0
+#define VG_ERR_INVALID_ARG (-1)        /* null pointer, bad value, misalignment      */
+#define VG_ERR_UNSUPPORTED_SHAPE (-2)  /* outside the shapes listed above             */
+#define VG_ERR_WORKSPACE (-3)          /* ws NULL or smaller than vg_workspace_size  */
+#define VG_ERR_CUDA (-4)               /* a CUDA runtime call failed                 */
+#define VG_ERR_DEVICE_TIMEOUT (-5)     /* device: a bounded wait ran out             */
+#define VG_ERR_DEVICE_BOUNDS (-6)      /* device: length or index out of range       */
+
+/* Problem dimensions (host struct). */
+typedef struct vg_dims {
+  int32_t B;       /* sequences in the batch                                          */
+  int32_t H_q;     /* query heads                                                     */
+  int32_t H_kv;    /* key/value heads; query head h reads KV head h / (H_q/H_kv)      */
+  int32_t d;       /* head dimension                                                  */
+  int32_t gamma;   /* draft tokens per iteration; verification has gamma+1 rows,     */
+                   /* row gamma being the bonus token (Vegas §2.B)                    */
+  int32_t max_len; /* host-side upper bound on every prefix length (sizes grids and  */
+                   /* the workspace; longer device lengths are reported, not read)   */
+  float scale;     /* logit scale; 0 means 1/sqrt(d)                                  */
+} vg_dims;
+
+/* The KV cache of one layer (host struct holding device pointers). */
+typedef struct vg_kv_cache {
+  void* K;                    /* bf16 [capacity_slots][H_kv][d]                       */
+  void* V;                    /* bf16 [capacity_slots][H_kv][d]                       */
+  const int64_t* seq_offset;  /* device int64 [B]: slot of token 0 of sequence b      */
+  int64_t capacity_slots;     /* slots in K and V                                     */
+} vg_kv_cache;
+
+/*
+ * Verification attention with fused logit aggregation (Vegas §2 step 1; §2.A; §2.B; §3).
+ *
+ * For sequence b with prefix length n_b = prefix_len[b], verify row t in [0, gamma]
+ * and query head h (KV head g = h / G):
+ *   out[b][t][h] = softmax_j(l_j) . V_j over j in {prefix 0..n_b-1} U {verify rows u <= t},
+ *   l_j = scale * q[b][t][h] . K_j   (causal among the verify rows, itself included);
+ * and for every prefix entry i < n_b and each enabled mask (row_mask0, row_mask1):
+ *   scores[b][i] = sum over rows t with bit t set, over all H_q heads, of
+ *                  scale * q[b][t][h] . K[seq_offset[b] + i][h / G]
+ * i.e. the objective of the Vegas §2.A selection formula, before any softmax.  The
+ * verify rows' own keys are not scored (T is a subset of the prefix P).
+ *
+ *   q        bf16 [B][gamma+1][H_q][d]
+ *   k_new    bf16 [B][gamma+1][H_kv][d] — the verify rows' keys and values.  They are
+ *   v_new        appended to the cache at slots seq_offset[b] + n_b + t.  Pass both
+ *                NULL when those slots already hold them.
+ *   prefix_len  device int32 [B], each in [0, max_len]
+ *   row_mask0/1 bit t selects verify row t; 0 disables that output.  Collect-2-Query
+ *               is (1 | 1 << gamma); all rows is (1 << (gamma+1)) - 1.
+ *   scores0/1   fp32 [B][score_stride] (score_stride >= max_len); NULL iff its mask is 0.
+ *               Entries at positions >= n_b are left untouched.
+ *   out      bf16 [B][gamma+1][H_q][d]
+ */
+vg_status vg_verify_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q,
+                         const void* k_new, const void* v_new, const int32_t* prefix_len,
+                         uint32_t row_mask0, uint32_t row_mask1, float* scores0, float* scores1,
+                         int64_t score_stride, void* out, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * Per-sequence top-k of the aggregated scores (Vegas §2 step 2, the argmax of §2.A).
+ *
+ * T_b = the k positions i < len[b] with the largest scores[b][i]; equal scores
+ * prefer the lower position; -0.0 equals +0.0 (NaN scores: unspecified order).
+ *   idx[b][0..count_b) = T_b in ascending order, count_b = min(k, len[b]);
+ *   idx[b][count_b..k) = -1;  count[b] = count_b.
+ *
+ *   scores  fp32 [B][score_stride];  len  device int32 [B], each in [0, max_len]
+ *   idx     int32 [B][k];            count  int32 [B]
+ * Uses no workspace (ws may be NULL).
+ */
+vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_t* len, int32_t B,
+                         int32_t max_len, int32_t k, int32_t* idx, int32_t* count, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * One sparse draft step (Vegas §2 step 3; §3 sparse execution with page size one).
+ *
+ * For sequence b the attended set is
+ *   A_b = { idx[b][j] : j < count[b] }  U  { tail_start[b] + u : u < tail_len[b] },
+ * positions relative to seq_offset[b].  out[b][h] = softmax over A_b of
+ * scale * q[b][h] . K_j, applied to V_j, on KV head h / G.
+ * If k_new / v_new (bf16 [B][H_kv][d]) are non-NULL they are the current draft
+ * token's key and value: they are appended at slot tail_start[b] + tail_len[b] - 1
+ * (tail_len[b] >= 1 is then required) and attended from the inputs directly.
+ * Selected positions must be < tail_start[b]; entries outside [0, tail_start[b]) are
+ * skipped and reported as VG_ERR_DEVICE_BOUNDS.
+ *
+ *   q      bf16 [B][H_q][d]             idx  int32 [B][k_stride], count int32 [B] (<= k_stride)
+ *   tail_start, tail_len  device int32 [B]   out  bf16 [B][H_q][d]
+ */
+vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q,
+                               const void* k_new, const void* v_new, const int32_t* idx,
+                               const int32_t* count, int32_t k_stride, const int32_t* tail_start,
+                               const int32_t* tail_len, void* out, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream);
+
+/* Inputs of one iteration (host struct of device pointers). */
+typedef struct vg_iter_inputs {
+  const void* q_verify;        /* bf16 [B][gamma+1][H_q][d]                              */
+  const void* k_verify;        /* bf16 [B][gamma+1][H_kv][d], appended at n_b + t         */
+  const void* v_verify;
+  const void* q_draft;         /* bf16 [gamma][B][H_q][d]                                */
+  const void* k_draft;         /* bf16 [gamma][B][H_kv][d]; step s appended at n_b + s    */
+  const void* v_draft;
+  const int32_t* prefix_len;   /* device int32 [B]                                       */
+} vg_iter_inputs;
+
+/* Outputs of one iteration (host struct of device pointers). */
+typedef struct vg_iter_outputs {
+  void* out_verify;            /* bf16 [B][gamma+1][H_q][d]                              */
+  float* scores0;              /* fp32 [B][score_stride], rows of row_mask0 (selection)   */
+  float* scores1;              /* fp32 [B][score_stride] or NULL (row_mask1 == 0)         */
+  int64_t score_stride;
+  int32_t* idx;                /* int32 [B][k]: selection on scores0                      */
+  int32_t* count;              /* int32 [B]                                              */
+  int32_t* idx1;               /* int32 [B][k] selection on scores1, or NULL              */
+  int32_t* count1;             /* int32 [B], or NULL                                     */
+  void* out_draft;             /* bf16 [gamma][B][H_q][d]                                */
+} vg_iter_outputs;
+
+/*
+ * One Vegas round (Vegas §2 steps 1-3), enqueued in order on `stream`:
+ *   vg_verify_attn (appends k_verify/v_verify) -> vg_topk_select on scores0
+ *   (and on scores1 if idx1 != NULL) -> for s = 0..gamma-1: vg_sparse_draft_attn
+ *   with q_draft[s], appending k_draft[s] at slot n_b + s and attending
+ *   T_b U {n_b .. n_b + s} (the draft tokens so far, the current one included).
+ * Draft tokens reuse the verify rows' slots.  k >= 1.
+ */
+vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in,
+                       int32_t k, uint32_t row_mask0, uint32_t row_mask1, vg_iter_outputs* out,
+                       void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Bytes of workspace any call above needs for these dimensions on the current
+ * device (0 on invalid dims or no device; see vg_last_error()). */
+size_t vg_workspace_size(const vg_dims* dims, int32_t k);
+
+/* Human-readable description of the last error on this host thread ("" if none). */
+const char* vg_last_error(void);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+int32_t vg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VG_H */

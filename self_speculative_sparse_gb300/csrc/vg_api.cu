@@ -1,0 +1,499 @@
+// Host side of the C ABI declared in include/vg.h: argument validation (before
+// any CUDA call, so bad arguments never touch the device), workspace carving,
+// TMA descriptor encoding and the launch sequence of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "vg.h"
+#include "vg_internal.h"
+
+namespace vg {
+namespace {
+
+thread_local std::string g_err;
+
+vg_status fail(vg_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+vg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(VG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device info
+struct DevInfo {
+  bool ok = false;
+  int sms = 0;
+  size_t smem_optin = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+vg_status device_info(DevInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(VG_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev[dev].ok) {
+    int sms = 0, optin = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_dev[dev].sms = sms;
+    g_dev[dev].smem_optin = static_cast<size_t>(optin);
+    g_dev[dev].ok = true;
+  }
+  *out = g_dev[dev];
+  return VG_OK;
+}
+
+// ---------------------------------------------------------------- TMA encode
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+vg_status get_encoder(EncodeTiledFn* fn) {
+  static std::once_flag once;
+  static EncodeTiledFn f = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) f = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!f) return fail(VG_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *fn = f;
+  return VG_OK;
+}
+
+// [capacity][Hkv*D] bf16 viewed as a 2-D tensor; boxes of 64 columns x 64 rows, 128-byte swizzle.
+vg_status encode_cache_map(CUtensorMap* map, void* base, int64_t capacity, int Hkv, int D) {
+  EncodeTiledFn enc;
+  vg_status st = get_encoder(&enc);
+  if (st != VG_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hkv) * D, static_cast<cuuint64_t>(capacity)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hkv) * D * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kVerifyTileKeys)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(VG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return VG_OK;
+}
+
+// ---------------------------------------------------------------- shapes
+struct Shape {
+  int B, Hq, Hkv, G, D, gamma, R, M, Mpad, max_len;
+  float scale;
+};
+
+vg_status check_dims(const vg_dims* d, Shape* s) {
+  if (!d) return fail(VG_ERR_INVALID_ARG, "dims is NULL");
+  if (d->B < 1 || d->B > kMaxBatch) return fail(VG_ERR_UNSUPPORTED_SHAPE, "B=%d outside [1, %d]", d->B, kMaxBatch);
+  if (d->H_kv < 1 || d->H_kv > 16) return fail(VG_ERR_UNSUPPORTED_SHAPE, "H_kv=%d outside [1, 16]", d->H_kv);
+  if (d->H_q < d->H_kv || d->H_q % d->H_kv != 0)
+    return fail(VG_ERR_INVALID_ARG, "H_q=%d is not a multiple of H_kv=%d", d->H_q, d->H_kv);
+  const int G = d->H_q / d->H_kv;
+  if (G > 16) return fail(VG_ERR_UNSUPPORTED_SHAPE, "group size %d > 16", G);
+  if (d->d != 64 && d->d != 128) return fail(VG_ERR_UNSUPPORTED_SHAPE, "head dim %d not in {64, 128}", d->d);
+  if (d->gamma < 0 || d->gamma > 15) return fail(VG_ERR_UNSUPPORTED_SHAPE, "gamma=%d outside [0, 15]", d->gamma);
+  const int R = d->gamma + 1;
+  if (G * R > 64) return fail(VG_ERR_UNSUPPORTED_SHAPE, "G*(gamma+1)=%d > 64", G * R);
+  if (d->max_len < 0) return fail(VG_ERR_INVALID_ARG, "max_len=%d < 0", d->max_len);
+  if (!(d->scale >= 0.f) || !std::isfinite(d->scale)) return fail(VG_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  s->B = d->B;
+  s->Hq = d->H_q;
+  s->Hkv = d->H_kv;
+  s->G = G;
+  s->D = d->d;
+  s->gamma = d->gamma;
+  s->R = R;
+  s->M = G * R;
+  s->Mpad = ((G * R + 15) / 16) * 16;
+  s->max_len = d->max_len;
+  s->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->d));
+  return VG_OK;
+}
+
+vg_status check_cache(const vg_kv_cache* c) {
+  if (!c) return fail(VG_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->K || !c->V || !c->seq_offset) return fail(VG_ERR_INVALID_ARG, "cache K, V and seq_offset must be non-NULL");
+  if (!aligned16(c->K) || !aligned16(c->V) || !aligned16(c->seq_offset))
+    return fail(VG_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (c->capacity_slots < 1 || c->capacity_slots > 0x7fffffffLL)
+    return fail(VG_ERR_INVALID_ARG, "capacity_slots=%lld outside [1, 2^31)", static_cast<long long>(c->capacity_slots));
+  return VG_OK;
+}
+
+vg_status check_mask(uint32_t mask, int R, const char* name) {
+  const uint32_t allowed = (R >= 32) ? 0xffffffffu : ((1u << R) - 1u);
+  if (mask & ~allowed) return fail(VG_ERR_INVALID_ARG, "%s=0x%x names a row beyond gamma", name, mask);
+  return VG_OK;
+}
+
+// ---------------------------------------------------------------- workspace
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t meta = 0, part_o = 0, part_ml = 0, part_s = 0;
+  size_t dmeta = 0, dpart_o = 0, dpart_ml = 0;
+  size_t total = 0;
+};
+
+WsLayout ws_layout(const Shape& s, int sms) {
+  WsLayout w;
+  const size_t segs = static_cast<size_t>(sms) + static_cast<size_t>(s.B) * s.Hkv;
+  size_t off = 0;
+  w.meta = off;
+  off = up256(off + (2 * static_cast<size_t>(s.B) + 1) * 4);
+  w.part_o = off;
+  off = up256(off + segs * s.Mpad * s.D * 4);
+  w.part_ml = off;
+  off = up256(off + segs * s.Mpad * 2 * 4);
+  w.part_s = off;
+  off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * static_cast<size_t>(s.max_len) * 4);
+  const size_t verify_total = off;
+  const size_t dsegs = static_cast<size_t>(sms) + s.B;
+  off = 0;  // the draft step's scratch reuses the same bytes (calls are stream-ordered)
+  w.dmeta = off;
+  off = up256(off + (static_cast<size_t>(s.B) + 1) * 4);
+  w.dpart_o = off;
+  off = up256(off + dsegs * s.Hq * s.D * 4);
+  w.dpart_ml = off;
+  off = up256(off + dsegs * s.Hq * 2 * 4);
+  w.total = verify_total > off ? verify_total : off;
+  return w;
+}
+
+vg_status check_ws(const Shape& s, const DevInfo& di, void* ws, size_t ws_bytes, WsLayout* w) {
+  *w = ws_layout(s, di.sms);
+  if (!ws) return fail(VG_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", w->total);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(VG_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < w->total) return fail(VG_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, w->total);
+  return VG_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------- verify
+struct VerifyArgs {
+  const void *q, *k_new, *v_new;
+  const int32_t* prefix_len;
+  uint32_t mask0, mask1;
+  float *scores0, *scores1;
+  int64_t score_stride;
+  void* out;
+};
+
+vg_status check_verify_args(const Shape& s, const VerifyArgs& a) {
+  if (!a.q || !a.prefix_len || !a.out) return fail(VG_ERR_INVALID_ARG, "q, prefix_len and out must be non-NULL");
+  if ((a.k_new == nullptr) != (a.v_new == nullptr)) return fail(VG_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+  if (!aligned16(a.q) || !aligned16(a.k_new) || !aligned16(a.v_new) || !aligned16(a.prefix_len) || !aligned16(a.out))
+    return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  vg_status st = check_mask(a.mask0, s.R, "row_mask0");
+  if (st != VG_OK) return st;
+  st = check_mask(a.mask1, s.R, "row_mask1");
+  if (st != VG_OK) return st;
+  if ((a.mask0 != 0) != (a.scores0 != nullptr)) return fail(VG_ERR_INVALID_ARG, "scores0 must be given iff row_mask0 != 0");
+  if ((a.mask1 != 0) != (a.scores1 != nullptr)) return fail(VG_ERR_INVALID_ARG, "scores1 must be given iff row_mask1 != 0");
+  if ((a.mask0 | a.mask1) && a.score_stride < s.max_len)
+    return fail(VG_ERR_INVALID_ARG, "score_stride=%lld < max_len=%d", static_cast<long long>(a.score_stride), s.max_len);
+  if (!aligned16(a.scores0) || !aligned16(a.scores1)) return fail(VG_ERR_INVALID_ARG, "scores must be 16-byte aligned");
+  return VG_OK;
+}
+
+vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, void* ws, const WsLayout& w,
+                     const DevInfo& di, int32_t* dev_status, cudaStream_t stream) {
+  if (verify_smem_bytes(s.D, s.Mpad, s.B) > di.smem_optin)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "verify needs %zu bytes of shared memory", verify_smem_bytes(s.D, s.Mpad, s.B));
+  CUtensorMap tmK, tmV;
+  vg_status st = encode_cache_map(&tmK, c->K, c->capacity_slots, s.Hkv, s.D);
+  if (st != VG_OK) return st;
+  st = encode_cache_map(&tmV, c->V, c->capacity_slots, s.Hkv, s.D);
+  if (st != VG_OK) return st;
+  VerifyParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  p.K = static_cast<__nv_bfloat16*>(c->K);
+  p.V = static_cast<__nv_bfloat16*>(c->V);
+  p.seq_offset = c->seq_offset;
+  p.prefix_len = a.prefix_len;
+  p.capacity = c->capacity_slots;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.G;
+  p.R = s.R;
+  p.D = s.D;
+  p.M = s.M;
+  p.Mpad = s.Mpad;
+  p.max_len = s.max_len;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.mask0 = a.mask0;
+  p.mask1 = a.mask1;
+  p.nctas = di.sms;
+  p.meta = at<int32_t>(ws, w.meta);
+  p.part_o = at<float>(ws, w.part_o);
+  p.part_ml = at<float>(ws, w.part_ml);
+  p.part_s = at<float>(ws, w.part_s);
+  p.scores0 = a.scores0;
+  p.scores1 = a.scores1;
+  p.score_stride = a.score_stride;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.status = dev_status;
+  cudaError_t e = launch_verify(p, tmK, tmV, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+  return VG_OK;
+}
+
+// ---------------------------------------------------------------- top-k
+vg_status check_topk_args(const float* scores, int64_t stride, const int32_t* len, int B, int max_len, int k,
+                          const int32_t* idx, const int32_t* count) {
+  if (!scores || !len || !idx || !count) return fail(VG_ERR_INVALID_ARG, "scores, len, idx and count must be non-NULL");
+  if (!aligned16(scores) || !aligned16(len) || !aligned16(idx) || !aligned16(count))
+    return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (B < 1 || B > kMaxBatch) return fail(VG_ERR_UNSUPPORTED_SHAPE, "B=%d outside [1, %d]", B, kMaxBatch);
+  if (max_len < 0 || max_len > kTopkMaxLen)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "max_len=%d outside [0, %d]", max_len, kTopkMaxLen);
+  if (k < 1) return fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
+  if (stride < max_len) return fail(VG_ERR_INVALID_ARG, "score_stride < max_len");
+  return VG_OK;
+}
+
+vg_status run_topk(const float* scores, int64_t stride, const int32_t* len, int B, int max_len, int k, int32_t* idx,
+                   int32_t* count, int32_t* dev_status, cudaStream_t stream, bool pdl) {
+  int C = (max_len + 16383) / 16384;
+  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  int per = (max_len + C - 1) / C;
+  per = ((per + 3) / 4) * 4;
+  if (per < 4) per = 4;
+  TopkParams p = {};
+  p.scores = scores;
+  p.score_stride = stride;
+  p.len = len;
+  p.B = B;
+  p.max_len = max_len;
+  p.k = k;
+  p.per_cta = per;
+  p.idx = idx;
+  p.count = count;
+  p.status = dev_status;
+  cudaError_t e = launch_topk(p, C, stream, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return VG_OK;
+}
+
+// ---------------------------------------------------------------- draft
+struct DraftArgs {
+  const void *q, *k_new, *v_new;
+  const int32_t *idx, *count;
+  int k_stride;
+  const int32_t *tail_start, *tail_len;
+  int tail_len_const;
+  void* out;
+};
+
+vg_status check_draft_args(const DraftArgs& a) {
+  if (!a.q || !a.idx || !a.count || !a.tail_start || !a.out)
+    return fail(VG_ERR_INVALID_ARG, "q, idx, count, tail_start and out must be non-NULL");
+  if ((a.k_new == nullptr) != (a.v_new == nullptr)) return fail(VG_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+  if (!aligned16(a.q) || !aligned16(a.k_new) || !aligned16(a.v_new) || !aligned16(a.idx) || !aligned16(a.count) ||
+      !aligned16(a.tail_start) || !aligned16(a.tail_len) || !aligned16(a.out))
+    return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if (a.k_stride < 1) return fail(VG_ERR_INVALID_ARG, "k_stride=%d < 1", a.k_stride);
+  return VG_OK;
+}
+
+vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, void* ws, const WsLayout& w,
+                    const DevInfo& di, int32_t* dev_status, cudaStream_t stream, bool pdl) {
+  const int stages = draft_stages(s.Hkv, s.D);
+  if (draft_smem_bytes(s.Hkv, s.D, stages, s.B) > di.smem_optin)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "draft needs too much shared memory");
+  DraftParams p = {};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  p.K = static_cast<__nv_bfloat16*>(c->K);
+  p.V = static_cast<__nv_bfloat16*>(c->V);
+  p.seq_offset = c->seq_offset;
+  p.capacity = c->capacity_slots;
+  p.idx = a.idx;
+  p.count = a.count;
+  p.k_stride = a.k_stride;
+  p.tail_start = a.tail_start;
+  p.tail_len = a.tail_len;
+  p.tail_len_const = a.tail_len_const;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.G = s.G;
+  p.D = s.D;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.nctas = di.sms;
+  p.stages = stages;
+  p.meta = at<int32_t>(ws, w.dmeta);
+  p.part_o = at<float>(ws, w.dpart_o);
+  p.part_ml = at<float>(ws, w.dpart_ml);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.status = dev_status;
+  cudaError_t e = launch_draft(p, stream, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "draft launch");
+  return VG_OK;
+}
+
+}  // namespace
+}  // namespace vg
+
+using namespace vg;
+
+extern "C" {
+
+int32_t vg_version(void) { return 100; }
+
+const char* vg_last_error(void) { return g_err.c_str(); }
+
+size_t vg_workspace_size(const vg_dims* dims, int32_t k) {
+  Shape s;
+  if (check_dims(dims, &s) != VG_OK) return 0;
+  if (k < 1) {
+    fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
+    return 0;
+  }
+  DevInfo di;
+  if (device_info(&di) != VG_OK) return 0;
+  g_err.clear();
+  return ws_layout(s, di.sms).total;
+}
+
+vg_status vg_verify_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q, const void* k_new,
+                         const void* v_new, const int32_t* prefix_len, uint32_t row_mask0, uint32_t row_mask1,
+                         float* scores0, float* scores1, int64_t score_stride, void* out, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream) {
+  g_err.clear();
+  Shape s;
+  vg_status st = check_dims(dims, &s);
+  if (st != VG_OK) return st;
+  if ((st = check_cache(cache)) != VG_OK) return st;
+  VerifyArgs a{q, k_new, v_new, prefix_len, row_mask0, row_mask1, scores0, scores1, score_stride, out};
+  if ((st = check_verify_args(s, a)) != VG_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0) return fail(VG_ERR_INVALID_ARG, "dev_status must be 4-byte aligned");
+  DevInfo di;
+  if ((st = device_info(&di)) != VG_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(s, di, ws, ws_bytes, &w)) != VG_OK) return st;
+  return run_verify(s, cache, a, ws, w, di, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_t* len, int32_t B, int32_t max_len,
+                         int32_t k, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, int32_t* dev_status,
+                         void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  g_err.clear();
+  vg_status st = check_topk_args(scores, score_stride, len, B, max_len, k, idx, count);
+  if (st != VG_OK) return st;
+  return run_topk(scores, score_stride, len, B, max_len, k, idx, count, dev_status,
+                  static_cast<cudaStream_t>(stream), true);
+}
+
+vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q, const void* k_new,
+                               const void* v_new, const int32_t* idx, const int32_t* count, int32_t k_stride,
+                               const int32_t* tail_start, const int32_t* tail_len, void* out, void* ws,
+                               size_t ws_bytes, int32_t* dev_status, void* stream) {
+  g_err.clear();
+  Shape s;
+  vg_status st = check_dims(dims, &s);
+  if (st != VG_OK) return st;
+  if ((st = check_cache(cache)) != VG_OK) return st;
+  if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
+  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
+  if ((st = check_draft_args(a)) != VG_OK) return st;
+  DevInfo di;
+  if ((st = device_info(&di)) != VG_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(s, di, ws, ws_bytes, &w)) != VG_OK) return st;
+  return run_draft(s, cache, a, ws, w, di, dev_status, static_cast<cudaStream_t>(stream), true);
+}
+
+vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in, int32_t k,
+                       uint32_t row_mask0, uint32_t row_mask1, vg_iter_outputs* out, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, void* stream) {
+  g_err.clear();
+  Shape s;
+  vg_status st = check_dims(dims, &s);
+  if (st != VG_OK) return st;
+  if ((st = check_cache(cache)) != VG_OK) return st;
+  if (!in || !out) return fail(VG_ERR_INVALID_ARG, "inputs and outputs must be non-NULL");
+  if (k < 1) return fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
+  if (row_mask0 == 0) return fail(VG_ERR_INVALID_ARG, "row_mask0 (the selection rows) must be non-zero");
+  if (s.max_len > kTopkMaxLen) return fail(VG_ERR_UNSUPPORTED_SHAPE, "max_len=%d > %d", s.max_len, kTopkMaxLen);
+  VerifyArgs va{in->q_verify, in->k_verify, in->v_verify, in->prefix_len, row_mask0, row_mask1,
+                out->scores0,  out->scores1,  out->score_stride, out->out_verify};
+  if ((st = check_verify_args(s, va)) != VG_OK) return st;
+  if (!out->idx || !out->count || !aligned16(out->idx) || !aligned16(out->count))
+    return fail(VG_ERR_INVALID_ARG, "idx and count must be non-NULL and 16-byte aligned");
+  if ((out->idx1 == nullptr) != (out->count1 == nullptr)) return fail(VG_ERR_INVALID_ARG, "idx1 and count1: both or neither");
+  if (out->idx1 && (!out->scores1 || !aligned16(out->idx1) || !aligned16(out->count1)))
+    return fail(VG_ERR_INVALID_ARG, "idx1 needs scores1 and 16-byte aligned idx1/count1");
+  if (s.gamma > 0) {
+    DraftArgs da{in->q_draft, in->k_draft, in->v_draft, out->idx, out->count, k, in->prefix_len, nullptr, 1,
+                 out->out_draft};
+    if (!in->k_draft || !in->v_draft) return fail(VG_ERR_INVALID_ARG, "k_draft and v_draft must be non-NULL");
+    if ((st = check_draft_args(da)) != VG_OK) return st;
+  }
+  DevInfo di;
+  if ((st = device_info(&di)) != VG_OK) return st;
+  WsLayout w;
+  if ((st = check_ws(s, di, ws, ws_bytes, &w)) != VG_OK) return st;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  if ((st = run_verify(s, cache, va, ws, w, di, dev_status, strm)) != VG_OK) return st;
+  if ((st = run_topk(out->scores0, out->score_stride, in->prefix_len, s.B, s.max_len, k, out->idx, out->count,
+                     dev_status, strm, true)) != VG_OK)
+    return st;
+  if (out->idx1 && (st = run_topk(out->scores1, out->score_stride, in->prefix_len, s.B, s.max_len, k, out->idx1,
+                                  out->count1, dev_status, strm, true)) != VG_OK)
+    return st;
+  const size_t qstep = static_cast<size_t>(s.B) * s.Hq * s.D * 2;
+  const size_t kvstep = static_cast<size_t>(s.B) * s.Hkv * s.D * 2;
+  for (int step = 0; step < s.gamma; ++step) {
+    DraftArgs da{static_cast<const char*>(in->q_draft) + step * qstep,
+                 static_cast<const char*>(in->k_draft) + step * kvstep,
+                 static_cast<const char*>(in->v_draft) + step * kvstep,
+                 out->idx,
+                 out->count,
+                 k,
+                 in->prefix_len,
+                 nullptr,
+                 step + 1,
+                 static_cast<char*>(out->out_draft) + step * qstep};
+    if ((st = run_draft(s, cache, da, ws, w, di, dev_status, strm, true)) != VG_OK) return st;
+  }
+  return VG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// Internal launch parameters and launchers of the Vegas kernels (host + device).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vg.h"
+
+namespace vg {
+
+// Keys per verify tile: the unit of TMA transfer and of the work split.
+constexpr int kVerifyTileKeys = 64;
+// Prefix positions per score-reduction block of the verify combine kernel.
+constexpr int kScoreChunk = 1024;
+// Positions per pipeline stage of the sparse draft kernel.
+constexpr int kDraftStageKeys = 16;
+// Largest sequence the top-k kernel holds in shared memory across a cluster of 8.
+constexpr int kTopkMaxLen = 262144;
+constexpr int kMaxBatch = 1024;
+
+struct VerifyParams {
+  const __nv_bfloat16* q;      // [B][R][Hq][D]
+  const __nv_bfloat16* k_new;  // [B][R][Hkv][D] or null (read from the cache)
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* K;            // cache [capacity][Hkv][D]
+  __nv_bfloat16* V;
+  const int64_t* seq_offset;   // [B]
+  const int32_t* prefix_len;   // [B]
+  int64_t capacity;
+  int B, Hq, Hkv, G, R, D, M, Mpad;  // M = G * R rows per KV head, Mpad = 16 * ceil(M / 16)
+  int max_len;
+  float scale;       // natural-log units (scores)
+  float scale_log2;  // scale * log2(e) (softmax)
+  uint32_t mask0, mask1;
+  int nctas;         // verify grid size
+  // workspace
+  int32_t* meta;     // [B + 1] tiles-per-head prefix sums, then [B] checked lengths
+  float* part_o;     // [nctas + B*Hkv][Mpad][D]  unnormalised partial outputs
+  float* part_ml;    // [nctas + B*Hkv][Mpad][2]  (running max in log2 units, sum)
+  float* part_s;     // [2][B][Hkv][max_len]       per-KV-head partial scores
+  // outputs
+  float* scores0;    // [B][score_stride] or null
+  float* scores1;
+  int64_t score_stride;
+  __nv_bfloat16* out;  // [B][R][Hq][D]
+  int32_t* status;
+};
+
+struct TopkParams {
+  const float* scores;
+  int64_t score_stride;
+  const int32_t* len;
+  int B, max_len, k;
+  int per_cta;  // positions held by one CTA of the cluster
+  int32_t* idx;
+  int32_t* count;
+  int32_t* status;
+};
+
+struct DraftParams {
+  const __nv_bfloat16* q;      // [B][Hq][D]
+  const __nv_bfloat16* k_new;  // [B][Hkv][D] or null
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* K;
+  __nv_bfloat16* V;
+  const int64_t* seq_offset;
+  int64_t capacity;
+  const int32_t* idx;          // [B][k_stride]
+  const int32_t* count;        // [B]
+  int k_stride;
+  const int32_t* tail_start;   // [B]
+  const int32_t* tail_len;     // [B] or null -> tail_len_const
+  int tail_len_const;
+  int B, Hq, Hkv, G, D;
+  float scale, scale_log2;
+  int nctas;
+  int stages;
+  int32_t* meta;               // [B + 1] entry prefix sums
+  float* part_o;               // [nctas + B][Hq][D]
+  float* part_ml;              // [nctas + B][Hq][2]
+  __nv_bfloat16* out;          // [B][Hq][D]
+  int32_t* status;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          cudaStream_t stream);
+size_t verify_smem_bytes(int D, int Mpad, int B);
+cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
+size_t topk_smem_bytes(int per_cta);
+cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
+int draft_stages(int Hkv, int D);
+size_t draft_smem_bytes(int Hkv, int D, int stages, int B);
+
+}  // namespace vg

@@ -1,0 +1,146 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Small cases that the oracle finishes in seconds but that still span several
+tiles, ragged tails, empty and one-entry prefixes, every m-tile count of the
+verify kernel (G*(gamma+1) = 16, 28, 32, 48, 64), both head dims, gamma = 0 and
+k >= n.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import synth  # noqa: E402
+from synth import Workload, scaled  # noqa: E402
+from tests.parity import bf16_to_f64, check_iteration, assert_attn_close  # noqa: E402
+
+import oracle  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from self_speculative_sparse_gb300 import build
+    build.build()
+
+
+CASES = {
+    "tiny": W["tiny"],
+    "llama8b_n1000": scaled(W["llama8b"], n=1000),
+    "batched_b3_n700": scaled(W["batched"], B=3, n=700),
+    "long70b_n2100": scaled(W["long70b"], n=2100),
+    "ragged_b6": scaled(W["loop32"], B=6, layers=1, ragged=(1, 1500)),
+    "g16_m64": Workload("g16", B=2, Hq=16, Hkv=1, d=128, gamma=3, k=100, n=777, seed=77),
+    "mha_d64_gamma0": Workload("mha", B=2, Hq=4, Hkv=4, d=64, gamma=0, k=33, n=200, seed=78),
+    "k_over_n": Workload("kbig", B=2, Hq=8, Hkv=2, d=64, gamma=2, k=300, n=250, seed=79),
+    "short_prefix": Workload("short", B=3, Hq=8, Hkv=4, d=128, gamma=5, k=8, n=None, ragged=(0, 70), seed=80),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_iteration_matches_oracle(name):
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = CASES[name]
+    pool = w.layer_pool(0)
+    st = LayerState(w, pool)
+    st.iteration()
+    torch.cuda.synchronize()
+    assert st.check_status() == 0, f"device status {st.check_status()}"
+    rows1 = w.rows(w.extra_rows) if w.extra_rows else None
+    check_iteration(w, pool, st, w.rows(w.select_rows), rows1)
+
+
+def test_iteration_is_deterministic():
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = CASES["batched_b3_n700"]
+    pool = w.layer_pool(0)
+    a = LayerState(w, pool)
+    a.iteration()
+    b = LayerState(w, pool)
+    b.iteration()
+    torch.cuda.synchronize()
+    for name in ("out_verify", "scores0", "scores1", "idx", "out_draft"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y), name
+
+
+def test_verify_reads_new_rows_from_cache_when_not_given():
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = CASES["llama8b_n1000"]
+    pool = w.layer_pool(0)
+    st = LayerState(w, pool)
+    st.verify(append=True)
+    torch.cuda.synchronize()
+    first = st.out_verify.clone()
+    s_first = st.scores0.clone()
+    st.out_verify.zero_()
+    st.verify(append=False)       # the rows are now in the cache
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), st.out_verify.view(torch.int16))
+    assert torch.equal(s_first, st.scores0)
+
+
+def test_topk_ties_signed_zero_and_edges():
+    from self_speculative_sparse_gb300 import binding as vb
+    rng = np.random.default_rng(3)
+    lens = [0, 1, 5, 1000, 40000, 70000]
+    B, L = len(lens), max(lens)
+    sc = np.zeros((B, L), dtype=np.float32)
+    for b, n in enumerate(lens):
+        v = rng.integers(-4, 5, size=n).astype(np.float32)          # heavy ties
+        v[v == 0] = np.where(rng.random((v == 0).sum()) < 0.5, -0.0, 0.0)
+        if b == 4:
+            v = rng.standard_normal(n).astype(np.float32) * 1e3     # spread values
+        sc[b, :n] = v
+    dev = torch.from_numpy(sc).cuda()
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k in (1, 3, 64, 5000, 100000):
+        idx = torch.full((B, k), 7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+        vb.vg_topk_select(dev, L, lt, B, L, k, idx, cnt, dev_status=status)
+        torch.cuda.synchronize()
+        gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+        for b, n in enumerate(lens):
+            want = oracle.select_topk(sc[b, :n].astype(np.float64), k)
+            m = min(k, n)
+            assert gc[b] == m, (k, b)
+            assert np.array_equal(gi[b, :m], want), (k, b)
+            assert (gi[b, m:] == -1).all(), (k, b)
+    assert int(status.item()) == 0
+
+
+def test_device_bounds_are_reported_not_faulted():
+    from self_speculative_sparse_gb300.runtime import LayerState
+    from self_speculative_sparse_gb300 import binding as vb
+    w = Workload("bad", B=2, Hq=8, Hkv=2, d=64, gamma=2, k=16, n=100, seed=81)
+    pool = w.layer_pool(0)
+    st = LayerState(w, pool)
+    st.prefix_len[1] = 100000          # beyond max_len and beyond the cache
+    st.verify()
+    torch.cuda.synchronize()
+    assert st.check_status() == vb.VG_ERR_DEVICE_BOUNDS
+    # sequence 0 is unaffected
+    K = oracle.widen_bf16(pool["K"][:100])
+    V = oracle.widen_bf16(pool["V"][:100])
+    ref = oracle.verify_attention(oracle.widen_bf16(pool["q_verify"][0]), K, V,
+                                  oracle.widen_bf16(pool["k_new"][0]), oracle.widen_bf16(pool["v_new"][0]))
+    assert_attn_close(bf16_to_f64(st.out_verify)[0], ref, "seq 0 after a bad seq 1")
+    # a draft index outside [0, tail_start) is skipped and reported
+    st2 = LayerState(w, pool)
+    st2.iteration()
+    torch.cuda.synchronize()
+    assert st2.check_status() == 0
+    st2.idx[0, 0] = 99999
+    st2.status.zero_()
+    tl = torch.full((w.B,), 1, dtype=torch.int32, device="cuda")
+    st2.draft_step(0, tl)
+    torch.cuda.synchronize()
+    assert st2.check_status() == vb.VG_ERR_DEVICE_BOUNDS
+    assert torch.isfinite(st2.out_draft[0].float()).all()
