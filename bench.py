@@ -1,0 +1,431 @@
+"""Benchmark of the Vegas hot path: one verify + select + gamma-step sparse-draft iteration.
+
+Default workload: one Llama-3-8B-shaped layer (B=1, H_q=32, H_kv=8, d=128,
+n=32768, gamma=7, k=2048, Collect-2-Query), synthetic heavy-hitter data.
+
+Timing discipline
+  * the KV cache is replicated into enough copies that all of them together are
+    larger than 4x L2; step i verifies + selects on copy i mod C and runs the gamma
+    draft steps on copy (i + C/2) mod C, so every kernel reads HBM cold and the
+    draft never profits from the verify pass that precedes it.  The draft uses
+    that copy's own selection (made earlier on identical data), which is the
+    method's order anyway: a draft phase follows the previous verification.
+  * W untimed warm-up steps, then K steps between CUDA events on the launching
+    stream, bracketed by a barrier and device synchronisation; rank 0 prints the
+    max over ranks.  Per-phase events inside the timed region give the verify
+    call's duration for the roofline figure.
+  * nvidia-smi samples clocks and throttle reasons during the timed region.
+
+`--impl reference` times the fp64 CPU oracle on the same workload (the only
+reference implementation there is); `--gpus N` under torchrun runs N independent
+replicas (the path has no data-path exchange: sequences are independent).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per verify+select+sparse-draft iteration"
+UNIT = "us/iteration"
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def workload_desc(w) -> str:
+    n = f"n={w.n}" if w.n is not None else f"n~U[{w.ragged[0]},{w.ragged[1]}]"
+    rows = "Collect-2-Query" if w.select_rows == "c2" else "all rows"
+    return (f"{w.name}: B={w.B} H_q={w.Hq} H_kv={w.Hkv} d={w.d} {n} gamma={w.gamma} k={w.k} "
+            f"select on {rows}" + (f" (+{w.extra_rows} overlap)" if w.extra_rows else "")
+            + (f", {w.layers} layers" if w.layers > 1 else ""))
+
+
+def algorithmic_bytes(w, lengths) -> dict:
+    """KV bytes one iteration must read: the prefix once for verify, k + s + 1 slots per draft step."""
+    per_tok = w.Hkv * w.d * 2 * 2
+    verify = int(sum(lengths)) * per_tok
+    draft = 0
+    for n in lengths:
+        cnt = min(w.k, int(n))
+        for s in range(w.gamma):
+            draft += (cnt + s + 1) * per_tok
+    return {"verify": verify, "draft": draft, "per_token": per_tok}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary, if it
+    was taken on the current source (the summary records the source's sha256)."""
+    src = os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", f"verify_attn_{workload}.md")
+    if not (os.path.exists(src) and os.path.exists(prof)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    vals = {}
+    for line in open(prof):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_iteration_time(w, pool, budget_s: float, max_reps: int = 1000):
+    """Time the fp64 oracle on whole iterations of sequence 0 of the workload."""
+    import numpy as np
+    import oracle
+    from oracle import widen_bf16
+    o, n = int(pool["seq_offset"][0]), int(pool["prefix_len"][0])
+    K, V = widen_bf16(pool["K"][o:o + n]), widen_bf16(pool["V"][o:o + n])
+    q = widen_bf16(pool["q_verify"][0])
+    kn, vn = widen_bf16(pool["k_new"][0]), widen_bf16(pool["v_new"][0])
+    qd, kd, vd = (widen_bf16(pool[x][:, 0]) for x in ("q_draft", "k_draft", "v_draft"))
+    rows0 = w.rows(w.select_rows)
+    rows1 = w.rows(w.extra_rows) if w.extra_rows else None
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        oracle.iteration(q, K, V, kn, vn, qd, kd, vd, w.k, rows0, rows1)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end:
+            break
+    return times
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank, world):
+    import synth
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    if w.layers > 1 or w.B > 1:
+        w_sample = synth.scaled(w, B=1, layers=1, n=int(w.lengths()[0]), ragged=None)
+    else:
+        w_sample = w
+    pool = w_sample.layer_pool(0)
+    for _ in range(args.warmup):
+        oracle_iteration_time(w_sample, pool, 0.0, max_reps=1)
+    times = []
+    for _ in range(args.steps):
+        times += oracle_iteration_time(w_sample, pool, 0.0, max_reps=1)
+    # one oracle iteration covers one sequence of one layer; scale to the workload
+    scale = w.B * w.layers if (w.layers > 1 or w.B > 1) else 1
+    per_iter_us = statistics.mean(times) * 1e6 * scale
+    sample = (f"{args.steps} oracle iterations of sequence 0 (n={int(pool['prefix_len'][0])}), "
+              f"scaled x{scale} to the workload" if scale > 1 else
+              f"{args.steps} full oracle iterations of the workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": per_iter_us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_iter_us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w)},
+        "cpu_baseline": {"value": per_iter_us, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": per_iter_us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, local, world):
+    import numpy as np
+    import torch
+    import synth
+    from self_speculative_sparse_gb300 import build as vbuild
+    from self_speculative_sparse_gb300 import binding as vb
+    from self_speculative_sparse_gb300.runtime import LayerState
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    vbuild.build()
+    w = synth.WORKLOADS[args.workload]
+    if w.layers > 1:
+        raise SystemExit("multi-layer workloads are timed by tests/test_gpu_fullsize.py, not bench.py")
+    pool = w.layer_pool(0)
+    lengths = pool["prefix_len"]
+    nbytes = algorithmic_bytes(w, lengths)
+    layer_bytes = int(pool["K"].nbytes + pool["V"].nbytes)
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    ncopy = max(3, -(-4 * l2 // layer_bytes) + 1)
+    states = [LayerState(w, pool, device=f"cuda:{local}") for _ in range(ncopy)]
+    stream = torch.cuda.current_stream()
+    tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device=f"cuda:{local}") for s in range(w.gamma)]
+
+    def draft_phase(st):  # on the current stream (the capture stream inside a graph capture)
+        for s in range(w.gamma):
+            st.draft_step(s, tl[s])
+
+    # every copy gets one full iteration first, so each has its own selection
+    for st in states:
+        st.iteration(stream=stream, select_extra=False)
+    torch.cuda.synchronize()
+    for st in states:
+        if st.check_status() != 0:
+            raise RuntimeError(f"device status {st.check_status()}")
+
+    # one CUDA graph per step kind and cache copy: a serving loop replays captured
+    # decode steps, so the host's launch cost stays off the GPU timeline
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn()
+        return g
+
+    half = ncopy // 2
+    g_step = [capture(lambda a=states[c], b=states[(c + half) % ncopy]: (a.verify(), a.select(), draft_phase(b)))
+              for c in range(ncopy)]
+    g_v = [capture(lambda st=st: st.verify()) for st in states]
+    g_s = [capture(lambda st=st: st.select()) for st in states]
+    g_d = [capture(lambda st=st: draft_phase(st)) for st in states]
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        g_step[i % ncopy].replay()
+    torch.cuda.synchronize()
+
+    # ---- headline: K back-to-back steps between two events
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        g_step[(args.warmup + i) % ncopy].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = e0.elapsed_time(e1)
+    # ---- per-phase events (same rotation) for the verify duration and the breakdown
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        c = (args.warmup + i) % ncopy
+        evs[i][0].record(stream)
+        g_v[c].replay()
+        evs[i][1].record(stream)
+        g_s[c].replay()
+        evs[i][2].record(stream)
+        g_d[(c + half) % ncopy].replay()
+        evs[i][3].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    t_verify = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    t_draft = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    for st in states:
+        if st.check_status() != 0:
+            raise RuntimeError(f"device status {st.check_status()}")
+
+    # ---- end to end through the public C ABI (vg_iteration) with host buffers
+    e2e_steps = args.e2e_steps or args.steps
+    host_in = {}
+    for name in ("q_verify", "k_new", "v_new", "q_draft", "k_draft", "v_draft"):
+        host_in[name] = getattr(states[0], name).cpu().pin_memory()
+    out_names = ("out_verify", "idx", "count", "out_draft")
+    host_out = {nm: torch.empty_like(getattr(states[0], nm), device="cpu").pin_memory() for nm in out_names}
+    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step(i):
+        a = states[i % ncopy]
+        for nm, t in host_in.items():
+            getattr(a, nm).copy_(t, non_blocking=True)
+        a.iteration(stream=stream, select_extra=False)
+        for nm, t in host_out.items():
+            t.copy_(getattr(a, nm), non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+
+    us_iter = ms_step * 1e3 / world  # whole-job: iterations of all ranks per unit time
+    peaks = measured_peaks()
+    verify_gbs = nbytes["verify"] / (t_verify * 1e-6) / 1e9
+    kv_gbs = (nbytes["verify"] + nbytes["draft"]) / (ms_step * 1e-3) / 1e9
+    launches_per_step = 2 + 1 + 2 * w.gamma
+    line = {
+        "metric": METRIC, "value": us_iter, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w),
+                   "l2": f"{ncopy} rotating cache copies of {layer_bytes / 1e6:.0f} MB (> 4x L2 of "
+                         f"{l2 / 1e6:.0f} MB); draft on a different copy than the verify before it",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_bytes_per_iteration": nbytes["verify"] + nbytes["draft"],
+        "kv_gbs": kv_gbs, "kv_pct_of_hbm": 100.0 * kv_gbs / peaks["hbm_gbs"],
+        "phases_us": {"verify_call": t_verify, "select": t_select, "draft_gamma_steps": t_draft,
+                      "per_draft_step": t_draft / max(1, w.gamma)},
+        "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine)", "bound": "hbm",
+                     "achieved": verify_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": verify_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "traffic": profiled_traffic("verify_attn.cu", w.name),
+                     "algorithmic_bytes": nbytes["verify"]},
+        "e2e": {"value": e2e_s / e2e_steps * 1e6 / world, "unit": UNIT, "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times = oracle_iteration_time(w, pool, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": statistics.mean(times) * 1e6, "unit": UNIT, "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{len(times)} full fp64 oracle iterations of the workload "
+                                          f"(verify, both score masks, top-k, {w.gamma} draft steps)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, local, world = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

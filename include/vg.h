@@ -46,7 +46,8 @@
  *
  * Shapes supported by this build: d in {64, 128}; H_kv in [1, 16]; H_q = G * H_kv
  * with G in [1, 16]; gamma in [0, 15]; G * (gamma+1) <= 64; 1 <= B <= 1024;
- * max_len <= 262144 for vg_topk_select; k >= 1.
+ * max_len <= 262144 for vg_topk_select; k >= 1; H_kv * d <= 1024 for
+ * vg_sparse_draft_attn (one token's page of K and of V is staged whole).
  */
 #ifndef VG_H
 #define VG_H
@@ -145,6 +146,7 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
  * If k_new / v_new (bf16 [B][H_kv][d]) are non-NULL they are the current draft
  * token's key and value: they are appended at slot tail_start[b] + tail_len[b] - 1
  * (tail_len[b] >= 1 is then required) and attended from the inputs directly.
+ * tail_len[b] <= 64; a longer tail is reported as VG_ERR_DEVICE_BOUNDS.
  * Selected positions must be < tail_start[b]; entries outside [0, tail_start[b]) are
  * skipped and reported as VG_ERR_DEVICE_BOUNDS.
  *

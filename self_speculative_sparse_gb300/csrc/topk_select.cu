@@ -9,8 +9,8 @@
 // GB300 design.  One thread-block cluster of up to 8 CTAs per sequence; each CTA
 // keeps its contiguous slice of the scores in shared memory as order-preserving
 // 32-bit keys.  An exact MSB-first radix select (4 passes of 8 bits) finds the
-// k-th largest key: every pass builds a CTA histogram (replicated 8x across banks
-// to tame same-bin conflicts), the cluster sums the histograms through
+// k-th largest key: every pass builds per-warp histograms with warp-aggregated
+// increments (no same-bin atomic conflicts), the cluster sums them through
 // distributed shared memory, and every CTA picks the same digit.  A final
 // cluster-wide exclusive scan in position order writes the selected positions,
 // taking the needed number of threshold-equal keys from the lowest positions.
@@ -27,7 +27,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRep = 8;  // histogram replicas (by lane % 8)
 
 // fp32 -> key with the same order; -0.0 is mapped to the key of +0.0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -36,42 +35,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of one int per thread; returns the total in *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += t;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? warp_sums[lane] : 0;
-    const int wv = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += t;
-    }
-    if (lane < kWarps) warp_sums[lane] = w - wv;
-    if (lane == 31) *total = w;
-  }
-  __syncthreads();
-  const int r = warp_sums[warp] + x - v;
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t tk_smem[];
   uint32_t* keys = tk_smem;                          // [per_cta]
-  uint32_t* hist = keys + p.per_cta;                 // [2][256 * kRep]
-  uint32_t* hsum = hist + 2 * 256 * kRep;            // [2][256]
+  uint32_t* hist = keys + p.per_cta;                 // [2][kWarps][256] per-warp histograms
+  uint32_t* hsum = hist + 2 * kWarps * 256;          // [2][256]
   int* wsum = reinterpret_cast<int*>(hsum + 2 * 256);  // [32]
-  int* misc = wsum + 32;                             // [8]
-  int* cnts = misc + 8;                              // [2]: this CTA's (#greater, #equal)
+  int* misc = wsum + 32;                             // [48]
+  int* cnts = misc + 48;                             // [2]: this CTA's (#greater, #equal)
   uint32_t* revc = reinterpret_cast<uint32_t*>(cnts + 2);  // [256] digit counts, highest first
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -103,7 +74,48 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int i = tid; i < mine; i += kThreads) out[start + i] = start + i;
     return;
   }
-  for (int i = tid; i < mine; i += kThreads) keys[i] = order_key(src[i]);
+  {
+    // batched loads: up to 8 independent loads in flight per thread per round
+    // (start is a multiple of 4 unless this is the ragged last CTA: then scalar)
+    const bool vec = (start & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+    if (vec) {
+      const int n4 = mine >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+      for (int base = 0; base < n4; base += 8 * kThreads) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i4 = base + q * kThreads + tid;
+          v[q] = i4 < n4 ? s4[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i4 = base + q * kThreads + tid;
+          if (i4 < n4) {
+            keys[4 * i4 + 0] = order_key(v[q].x);
+            keys[4 * i4 + 1] = order_key(v[q].y);
+            keys[4 * i4 + 2] = order_key(v[q].z);
+            keys[4 * i4 + 3] = order_key(v[q].w);
+          }
+        }
+      }
+      for (int i = (n4 << 2) + tid; i < mine; i += kThreads) keys[i] = order_key(src[i]);
+    } else {
+      for (int base = 0; base < mine; base += 8 * kThreads) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = base + q * kThreads + tid;
+          v[q] = i < mine ? src[i] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = base + q * kThreads + tid;
+          if (i < mine) keys[i] = order_key(v[q]);
+        }
+      }
+    }
+  }
 
   // ---------------------------------------------------------------- radix select
   uint32_t prefix = 0u, pmask = 0u;
@@ -111,18 +123,26 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     const int hb = pass & 1;
-    uint32_t* h = hist + hb * 256 * kRep;
-    for (int i = tid; i < 256 * kRep; i += kThreads) h[i] = 0u;
+    uint32_t* h = hist + hb * kWarps * 256;
+    for (int i = tid; i < kWarps * 256; i += kThreads) h[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < mine; i += kThreads) {
-      const uint32_t key = keys[i];
-      if ((key & pmask) == prefix) atomicAdd(&h[((key >> shift) & 255u) * kRep + (lane & (kRep - 1))], 1u);
+    // warp-aggregated counting: lanes with the same digit add once, into their
+    // warp's own histogram, so concentrated digits cause no atomic conflicts
+    uint32_t* hw = h + (tid >> 5) * 256;
+    const int rounds = (mine + kThreads - 1) / kThreads;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int i = rd * kThreads + tid;
+      const uint32_t key = i < mine ? keys[i] : 0u;
+      const bool cand = i < mine && (key & pmask) == prefix;
+      const uint32_t dg = cand ? ((key >> shift) & 255u) : 256u;
+      const unsigned peers = __match_any_sync(0xffffffffu, dg);
+      if (cand && lane == __ffs(peers) - 1) atomicAdd(&hw[dg], static_cast<uint32_t>(__popc(peers)));
     }
     __syncthreads();
     if (tid < 256) {
       uint32_t s = 0;
 #pragma unroll
-      for (int c = 0; c < kRep; ++c) s += h[tid * kRep + c];
+      for (int w = 0; w < kWarps; ++w) s += h[w * 256 + tid];
       hsum[hb * 256 + tid] = s;
     }
     cluster.sync();
@@ -173,24 +193,49 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   const uint32_t thr = prefix;  // k-th largest key; `remaining` keys equal to it are taken
 
   // ---------------------------------------------------------------- compaction
-  // thread t owns the contiguous run [t*E, (t+1)*E) of this CTA's slice
-  const int E = (mine + kThreads - 1) / kThreads;
-  const int i0 = min(mine, tid * E), i1 = min(mine, i0 + E);
+  // Warp w owns the contiguous run [w0, w1) of this CTA's slice; within a run, 32
+  // consecutive keys are handled per step (conflict-free shared reads) and ballots
+  // give each selected position its output slot in position order.
+  const int warp = tid >> 5;
+  const int WR = ((mine + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = min(mine, warp * WR), w1 = min(mine, w0 + WR);
   int ngt = 0, neq = 0;
-  for (int i = i0; i < i1; ++i) {
+  for (int i = w0 + lane; i < w1; i += 32) {
     const uint32_t key = keys[i];
     ngt += key > thr;
     neq += key == thr;
   }
-  int cta_gt = 0, cta_eq = 0;
-  const int gt_before = block_exclusive_scan(ngt, wsum, &misc[2]);
-  cta_gt = misc[2];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
+    neq += __shfl_xor_sync(0xffffffffu, neq, o);
+  }
+  if (lane == 0) {
+    wsum[warp] = ngt;
+    wsum[kWarps + warp] = neq;
+  }
   __syncthreads();
-  const int eq_before = block_exclusive_scan(neq, wsum, &misc[3]);
-  cta_eq = misc[3];
-  if (tid == 0) {
-    cnts[0] = cta_gt;
-    cnts[1] = cta_eq;
+  if (warp == 0) {  // exclusive scans over the warps' runs, and this CTA's totals
+    const int g = lane < kWarps ? wsum[lane] : 0;
+    const int e = lane < kWarps ? wsum[kWarps + lane] : 0;
+    int gi = g, ei = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int tg = __shfl_up_sync(0xffffffffu, gi, o);
+      const int te = __shfl_up_sync(0xffffffffu, ei, o);
+      if (lane >= o) {
+        gi += tg;
+        ei += te;
+      }
+    }
+    if (lane < kWarps) {
+      misc[8 + lane] = gi - g;   // greater keys before warp `lane`'s run
+      misc[24 + lane] = ei - e;  // equal keys before it
+    }
+    if (lane == kWarps - 1) {
+      cnts[0] = gi;
+      cnts[1] = ei;
+    }
   }
   cluster.sync();
   int off = 0, eq_prev = 0, take_mine = 0;
@@ -203,34 +248,34 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     eq_prev += e_r;
   }
   cluster.sync();  // no CTA leaves while its counters may still be read
-  (void)gt_before;
-  // selected count before my run: greater keys before + equal keys taken before
-  const int sel_before = gt_before + min(eq_before, take_mine);
-  int pos = off + sel_before;
+  const int gt_before = misc[8 + warp], eq_before = misc[24 + warp];
+  int sel_base = off + gt_before + min(eq_before, take_mine);
   int eq_rank = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = keys[i];
-    bool sel = key > thr;
-    if (key == thr) {
-      sel = eq_rank < take_mine;
-      ++eq_rank;
-    }
-    if (sel) out[pos++] = start + i;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < w1;
+    const uint32_t key = valid ? keys[i] : 0u;
+    const bool gt = valid && key > thr;
+    const bool eq = valid && key == thr;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool sel = gt || (eq && eq_rank + __popc(eqm & lt) < take_mine);
+    const unsigned selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) out[sel_base + __popc(selm & lt)] = start + i;
+    sel_base += __popc(selm);
+    eq_rank += __popc(eqm);
   }
 }
 
 }  // namespace
 
 size_t topk_smem_bytes(int per_cta) {
-  return static_cast<size_t>(per_cta) * 4 + (2 * 256 * kRep + 2 * 256) * 4 + (32 + 8 + 2 + 256) * 4;
+  return static_cast<size_t>(per_cta) * 4 + (2 * kWarps * 256 + 2 * 256) * 4 + (32 + 48 + 2 + 256) * 4;
 }
 
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl) {
   const size_t smem = topk_smem_bytes(p.per_cta);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = ensure_smem<topk_kernel>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, p.B);

@@ -9,19 +9,20 @@
 //
 // GB300 design.  The work is the flattened list of (sequence, KV head, 64-key tile)
 // items, split evenly over one persistent CTA per SM (ragged batches balance by
-// construction).  In each CTA a producer warp streams K and V tiles with 2-D TMA
+// construction).  Thread 0 of each CTA streams K and V tiles with 2-D TMA
 // (128-byte swizzled boxes) into a 5-stage shared-memory ring guarded by
-// mbarriers; the consumer warps hold the G*(gamma+1) query rows of the current KV
-// head as tensor-core fragments and run QK^T and PV on bf16 MMA with fp32
-// accumulators and an online softmax.  The logit sums are taken from the same QK^T
-// fragments, so the cache is read exactly once.  Each contiguous run of tiles of one
-// (sequence, KV head) leaves one unnormalised partial (max, sum, O); a small
+// mbarriers; 8 or 12 warps hold the G*(gamma+1) query rows of the current KV head
+// as tensor-core fragments and run QK^T and PV on bf16 MMA with fp32
+// accumulators and an online softmax.  The logit sums are taken from the same
+// QK^T fragments, so the cache is read exactly once.  Each contiguous run of tiles
+// of one (sequence, KV head) leaves one unnormalised partial (max, sum, O); a
 // combine kernel, launched as a programmatic dependent of this one, merges the
 // partials with the verify rows' own causal keys, writes bf16 outputs, appends the
 // verify rows' K/V to the cache and sums the per-KV-head partial scores in a fixed
 // order (deterministic, no atomics).
-#include <cooperative_groups.h>
+#include <cstdio>
 
+#include "attn_frag.cuh"
 #include "vg_common.cuh"
 #include "vg_internal.h"
 
@@ -35,20 +36,20 @@ template <int D, int MT>
 struct VCfg {
   static constexpr int KGW = (MT == 4) ? 2 : 4;  // key-group warps per 16-row m-tile
   static constexpr int KPW = 4 / KGW;            // 16-key groups per warp per tile
-  static constexpr int W = MT * KGW;             // consumer warps
-  static constexpr int THREADS = (W + 1) * 32;   // + one producer warp
-  static constexpr int MAXREG = (65536 / THREADS) / 8 * 8 > 255 ? 255 : (65536 / THREADS) / 8 * 8;
+  static constexpr int W = MT * KGW;             // warps (a multiple of 4: one share per SM sub-partition)
+  static constexpr int THREADS = W * 32;
   static constexpr int HALVES = D / 64;          // 64-column (128-byte) swizzled boxes
   static constexpr int HALF_BYTES = TK * 128;
   static constexpr int TILE_BYTES = TK * D * 2;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int M = MT * 16;
-  static constexpr int OFF_MERGE = kStages * STAGE_BYTES;   // float [M][D]
-  static constexpr int OFF_MROW = OFF_MERGE + M * D * 4;    // float [KGW][M]
-  static constexpr int OFF_LROW = OFF_MROW + KGW * M * 4;   // float [M]
-  static constexpr int OFF_SC = OFF_LROW + M * 4;           // float [2 buf][2 mask][MT][TK]
-  static constexpr int OFF_BAR = OFF_SC + 2 * 2 * MT * TK * 4;
-  static constexpr int OFF_META = OFF_BAR + 2 * kStages * 8;  // int cum[B+1], nlen[B]
+  static constexpr int MSTRIDE = D + 8;                        // padded merge rows: 2-way at most
+  static constexpr int OFF_MERGE = kStages * STAGE_BYTES;      // float [M][MSTRIDE]
+  static constexpr int OFF_MROW = OFF_MERGE + M * MSTRIDE * 4; // float [KGW][M]
+  static constexpr int OFF_LROW = OFF_MROW + KGW * M * 4;      // float [M]
+  static constexpr int OFF_CNT = OFF_LROW + M * 4;             // uint32 [kStages] warps done per stage
+  static constexpr int OFF_BAR = (OFF_CNT + kStages * 4 + 7) & ~7;
+  static constexpr int OFF_META = OFF_BAR + kStages * 8;       // int cum[B+1], nlen[B]
   static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
 };
 
@@ -111,7 +112,7 @@ __device__ __forceinline__ void advance(int& b, int& g, int& j, const int* cum, 
 }
 
 template <int D, int MT>
-__global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, MT>::MAXREG))
+__global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
     verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
   using C = VCfg<D, MT>;
@@ -120,9 +121,8 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
   float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
   float* mrow = reinterpret_cast<float*>(smem + C::OFF_MROW);
   float* lrow = reinterpret_cast<float*>(smem + C::OFF_LROW);
-  float* sc = reinterpret_cast<float*>(smem + C::OFF_SC);
+  uint32_t* done = reinterpret_cast<uint32_t*>(smem + C::OFF_CNT);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kStages;
   int* cum = reinterpret_cast<int*>(smem + C::OFF_META);
   int* nlen = cum + p.B + 1;
 
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::W);
+      done[s] = 0u;
     }
     fence_mbar_init();
   }
@@ -146,38 +146,30 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
   const int t1 = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas));
   if (t0 >= t1) return;
 
-  // ------------------------------------------------------------ producer warp
-  if (warp == C::W) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      int b, g, j;
-      locate(t0, cum, p.B, p.Hkv, b, g, j);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int x = t0; x < t1; ++x) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, p.status)) break;
-        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-        uint8_t* kdst = smem + stage * C::STAGE_BYTES;
-        uint8_t* vdst = kdst + C::TILE_BYTES;
-        const int y = static_cast<int>(p.seq_offset[b] + static_cast<int64_t>(j) * TK);
+  // The ring holds tiles x .. x + kStages - 1.  Thread 0 fills it first; afterwards
+  // the last warp to finish a tile refills that stage with tile x + kStages, so no
+  // warp ever waits for the others between tiles.
+  auto issue = [&](int stage, int tile) {
+    int ib, ig, ij;
+    locate(tile, cum, p.B, p.Hkv, ib, ig, ij);
+    fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
+    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+    uint8_t* kdst = smem + stage * C::STAGE_BYTES;
+    uint8_t* vdst = kdst + C::TILE_BYTES;
+    const int y = static_cast<int>(p.seq_offset[ib] + static_cast<int64_t>(ij) * TK);
 #pragma unroll
-        for (int h = 0; h < C::HALVES; ++h) {
-          tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, g * D + h * 64, y, &full[stage]);
-          tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, g * D + h * 64, y, &full[stage]);
-        }
-        if (x + 1 < t1) advance(b, g, j, cum, p.B, p.Hkv);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
+    for (int h = 0; h < C::HALVES; ++h) {
+      tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, ig * D + h * 64, y, &full[stage]);
+      tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, ig * D + h * 64, y, &full[stage]);
     }
-    return;
+  };
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    for (int st = 0; st < kStages && t0 + st < t1; ++st) issue(st, t0 + st);
   }
 
-  // ------------------------------------------------------------ consumer warps
-  constexpr int NT = C::W * 32;
+  constexpr int NT = C::THREADS;
   const int mt = warp % MT, kgw = warp / MT;
   const int gid = lane >> 2, tig = lane & 3;
   const int row0 = mt * 16 + gid, row1 = row0 + 8;
@@ -190,7 +182,7 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
 
   int b, g, j;
   locate(t0, cum, p.B, p.Hkv, b, g, j);
-  int stage = 0, it = 0;
+  int stage = 0;
   uint32_t phase = 0;
   bool lost = false;
   int x = t0;
@@ -199,52 +191,52 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
     const int seg_end = min(t1, x + (tiles_b - j));
     const int n_b = nlen[b];
 
-    // query rows of this (sequence, KV head) as A fragments: row m -> (t = m / G, head g*G + m % G)
+    // query rows of this (sequence, KV head): row m -> (t = m / G, head g*G + m % G)
     uint32_t qf[D / 16][4];
-    {
-      const __nv_bfloat16* q0 = nullptr;
-      const __nv_bfloat16* q1 = nullptr;
-      if (row0 < p.M) q0 = p.q + ((static_cast<size_t>(b) * p.R + vt0) * p.Hq + g * p.G + row0 % p.G) * D;
-      if (row1 < p.M) q1 = p.q + ((static_cast<size_t>(b) * p.R + vt1) * p.Hq + g * p.G + row1 % p.G) * D;
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int c0 = ks * 16 + tig * 2;
-        qf[ks][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + c0) : 0u;
-        qf[ks][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + c0) : 0u;
-        qf[ks][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + c0 + 8) : 0u;
-        qf[ks][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + c0 + 8) : 0u;
-      }
-    }
-    float m_run[2] = {NEG, NEG}, l_run[2] = {0.f, 0.f};
-    float o[D / 8][4];
-#pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+    load_q_frags<D>(qf,
+                    row0 < p.M ? p.q + ((static_cast<size_t>(b) * p.R + vt0) * p.Hq + g * p.G + row0 % p.G) * D
+                               : nullptr,
+                    row1 < p.M ? p.q + ((static_cast<size_t>(b) * p.R + vt1) * p.Hq + g * p.G + row1 % p.G) * D
+                               : nullptr,
+                    tig);
+    RowState<D> st;
+    st.init();
 
-    for (; x < seg_end; ++x, ++j, ++it) {
+    for (; x < seg_end; ++x, ++j) {
       if (!mbar_wait(&full[stage], phase, p.status)) {
         lost = true;
         break;
       }
+      const int valid = n_b - j * TK;  // keys of this tile inside the prefix
+      if (valid < TK) {  // (at most once per run of tiles, the only point where warps meet)
+        // The rows past the prefix end hold whatever the cache has there; their
+        // probabilities are zero, and zeroed values keep 0 * V exact even if the
+        // slots hold non-finite garbage.
+        uint4* vrows = reinterpret_cast<uint4*>(smem + stage * C::STAGE_BYTES + C::TILE_BYTES);
+        const int per_half = TK * 8;  // 16-byte chunks in one 128-byte-wide box
+        for (int e = threadIdx.x; e < C::HALVES * per_half; e += NT) {
+          const int h = e / per_half, r = (e - h * per_half) >> 3;
+          if (r >= valid) vrows[e] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // before the next TMA write into this stage
+        named_bar(2, NT);
+      }
       const uint32_t kb = smem_u32(smem + stage * C::STAGE_BYTES);
       const uint32_t vb = kb + C::TILE_BYTES;
-      float* scb = sc + (it & 1) * (2 * MT * TK);
 #pragma unroll
       for (int kp = 0; kp < C::KPW; ++kp) {
         const int kg = kgw * C::KPW + kp;
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int r = kg * 16 + (mi >> 1) * 8 + rr;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int c16 = ks * 2 + (mi & 1);
-            const uint32_t addr = kb + (c16 >> 3) * C::HALF_BYTES + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
-            mma_bf16(s[0], qf[ks], b0, b1);
-            mma_bf16(s[1], qf[ks], b2, b3);
-          }
-        }
+        // 128-byte swizzle of the TMA boxes: chunk c of row r sits at chunk c ^ (r & 7)
+        auto kaddr = [&](int r, int c16) {
+          const int rr = kg * 16 + r;
+          return kb + (c16 >> 3) * C::HALF_BYTES + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4);
+        };
+        auto vaddr = [&](int r, int c16) {
+          const int rr = kg * 16 + r;
+          return vb + (c16 >> 3) * C::HALF_BYTES + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4);
+        };
+        float s[2][4];
+        qk16<D>(qf, kaddr, s, lane);
         const int key0 = j * TK + kg * 16;
         if (any_mask) {  // logit sums over this warp's rows of each mask, then over lanes sharing a key
           float v0[4], v1[4];
@@ -264,18 +256,22 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
               v1[i] += __shfl_xor_sync(0xffffffffu, v1[i], off);
             }
           }
-          if (gid == 0) {
+          if (gid == 0) {  // this m-tile's share of the KV head's score of each key
+            float* s0 = p.part_s + (((static_cast<size_t>(0) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len;
+            float* s1 = p.part_s + (((static_cast<size_t>(1) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
-                const int col = kg * 16 + nt * 8 + tig * 2 + c;
-                scb[(0 * MT + mt) * TK + col] = v0[nt * 2 + c] * p.scale;
-                scb[(1 * MT + mt) * TK + col] = v1[nt * 2 + c] * p.scale;
+                const int pos = key0 + nt * 8 + tig * 2 + c;
+                if (pos < n_b) {
+                  if (p.mask0) s0[pos] = v0[nt * 2 + c] * p.scale;
+                  if (p.mask1) s1[pos] = v1[nt * 2 + c] * p.scale;
+                }
               }
           }
         }
-        // online softmax in log2 units; keys past the prefix end are masked
+        // softmax in log2 units; keys past the prefix end are masked
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -284,140 +280,27 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
             s[nt][c] = ok ? s[nt][c] * p.scale_log2 : NEG;
             s[nt][2 + c] = ok ? s[nt][2 + c] * p.scale_log2 : NEG;
           }
-        float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-        const float mu0 = mn0 == NEG ? 0.f : mn0, mu1 = mn1 == NEG ? 0.f : mn1;
-        if (__any_sync(0xffffffffu, (mn0 > m_run[0]) || (mn1 > m_run[1]))) {
-          const float a0 = ex2(m_run[0] - mu0), a1 = ex2(m_run[1] - mu1);
-          l_run[0] *= a0;
-          l_run[1] *= a1;
-#pragma unroll
-          for (int dn = 0; dn < D / 8; ++dn) {
-            o[dn][0] *= a0;
-            o[dn][1] *= a0;
-            o[dn][2] *= a1;
-            o[dn][3] *= a1;
-          }
-        }
-        m_run[0] = mn0;
-        m_run[1] = mn1;
-        float pr[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          pr[nt][0] = ex2(s[nt][0] - mu0);
-          pr[nt][1] = ex2(s[nt][1] - mu0);
-          pr[nt][2] = ex2(s[nt][2] - mu1);
-          pr[nt][3] = ex2(s[nt][3] - mu1);
-        }
-        l_run[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
-        l_run[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-        const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
-                                pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
-        {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int r = kg * 16 + (mi & 1) * 8 + rr;
-#pragma unroll
-          for (int dn2 = 0; dn2 < D / 16; ++dn2) {
-            const int c16 = dn2 * 2 + (mi >> 1);
-            const uint32_t addr = vb + (c16 >> 3) * C::HALF_BYTES + r * 128 + (((c16 & 7) ^ (r & 7)) << 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
-            mma_bf16(o[2 * dn2], pa, b0, b1);
-            mma_bf16(o[2 * dn2 + 1], pa, b2, b3);
-          }
-        }
+        softmax_pv16<D>(st, s, vaddr, lane);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (lane == 0) {  // the last warp done with this stage refills it
+        if (atom_add_acq_rel_smem(&done[stage], 1u) == C::W - 1) {
+          done[stage] = 0u;
+          if (x + kStages < t1) issue(stage, x + kStages);
+        }
+      }
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
-      if (any_mask) {  // per-KV-head partial score of each key: sum over the m-tiles
-        named_bar(1, NT);
-        for (int e = threadIdx.x; e < 2 * TK; e += NT) {
-          const int ms = e / TK, col = e - ms * TK;
-          if ((ms ? p.mask1 : p.mask0) == 0u) continue;
-          const int pos = j * TK + col;
-          if (pos < n_b) {
-            float v = 0.f;
-#pragma unroll
-            for (int m2 = 0; m2 < MT; ++m2) v += scb[(ms * MT + m2) * TK + col];
-            p.part_s[((static_cast<size_t>(ms) * p.B + b) * p.Hkv + g) * p.max_len + pos] = v;
-          }
-        }
-      }
     }
 
-    // ---------------------------------------------------- segment partial
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 1);
-    l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], 2);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 1);
-    l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], 2);
-    if (tig == 0) {
-      mrow[kgw * C::M + row0] = m_run[0];
-      mrow[kgw * C::M + row1] = m_run[1];
-    }
+    // segment partial: merge the key-group warps of each m-tile, then store
+    merge_warps<D, C::KGW>(st, C::M, C::MSTRIDE, row0, kgw, merge, mrow, lrow, tig, 1, NT);
+    const size_t id = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g;
+    store_partial<D, C::KGW>(merge, C::MSTRIDE, mrow, lrow, C::M, p.part_o + id * C::M * D,
+                             p.part_ml + id * C::M * 2, threadIdx.x, NT);
     named_bar(1, NT);
-    float mf0 = NEG, mf1 = NEG;
-#pragma unroll
-    for (int w2 = 0; w2 < C::KGW; ++w2) {
-      mf0 = fmaxf(mf0, mrow[w2 * C::M + row0]);
-      mf1 = fmaxf(mf1, mrow[w2 * C::M + row1]);
-    }
-    {
-      const float f0 = ex2(m_run[0] - (mf0 == NEG ? 0.f : mf0));
-      const float f1 = ex2(m_run[1] - (mf1 == NEG ? 0.f : mf1));
-      l_run[0] *= f0;
-      l_run[1] *= f1;
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        o[dn][0] *= f0;
-        o[dn][1] *= f0;
-        o[dn][2] *= f1;
-        o[dn][3] *= f1;
-      }
-    }
-    for (int w2 = 0; w2 < C::KGW; ++w2) {  // fixed order: deterministic sums
-      if (kgw == w2) {
-#pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-          float2* d0 = reinterpret_cast<float2*>(merge + row0 * D + dn * 8 + tig * 2);
-          float2* d1 = reinterpret_cast<float2*>(merge + row1 * D + dn * 8 + tig * 2);
-          if (w2 == 0) {
-            *d0 = make_float2(o[dn][0], o[dn][1]);
-            *d1 = make_float2(o[dn][2], o[dn][3]);
-          } else {
-            float2 a = *d0, c = *d1;
-            *d0 = make_float2(a.x + o[dn][0], a.y + o[dn][1]);
-            *d1 = make_float2(c.x + o[dn][2], c.y + o[dn][3]);
-          }
-        }
-        if (tig == 0) {
-          lrow[row0] = (w2 == 0 ? 0.f : lrow[row0]) + l_run[0];
-          lrow[row1] = (w2 == 0 ? 0.f : lrow[row1]) + l_run[1];
-        }
-      }
-      named_bar(1, NT);
-    }
-    {
-      const size_t id = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g;
-      float4* dst = reinterpret_cast<float4*>(p.part_o + id * C::M * D);
-      const float4* src = reinterpret_cast<const float4*>(merge);
-      for (int e = threadIdx.x; e < C::M * D / 4; e += NT) dst[e] = src[e];
-      for (int r = threadIdx.x; r < C::M; r += NT) {
-        float mf = NEG;
-        for (int w2 = 0; w2 < C::KGW; ++w2) mf = fmaxf(mf, mrow[w2 * C::M + r]);
-        p.part_ml[(id * C::M + r) * 2 + 0] = mf;
-        p.part_ml[(id * C::M + r) * 2 + 1] = lrow[r];
-      }
-      named_bar(1, NT);
-    }
     if (x < t1) {  // next (sequence, KV head)
       j = 0;
       if (++g == p.Hkv) {
@@ -430,9 +313,18 @@ __global__ void __launch_bounds__((VCfg<D, MT>::THREADS)) __maxnreg__((VCfg<D, M
 }
 
 // Merge of the partials with the verify rows' causal keys, output, append, scores.
+// Role A, one CTA per (sequence b, KV head g, verify row t): its G query rows.
+//   phase 1: every (segment, row) max/sum into shared memory (one round trip);
+//   phase 2: one warp per row, lanes across d, independent loads over segments.
+// Role B, one CTA per (sequence, 1024 positions): fixed-order sum of the per-KV-head
+// partial scores.
 template <int D>
 __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams p) {
-  __shared__ float lg[16][16];  // [head in group][verify row u] logits, log2 units
+  extern __shared__ float cs[];                  // [nctas][G] max, [nctas][G] sum
+  __shared__ float lg[16][16];                   // [row in group][verify key u] logits, log2 units
+  __shared__ __align__(16) __nv_bfloat16 qs[16][D];  // this verify row's G query rows
+  __shared__ __align__(16) __nv_bfloat16 ks[16][D];  // the verify rows' own keys u <= t
+  __shared__ __align__(16) __nv_bfloat16 vs[16][D];  // ... and values
   pdl_wait();
   const int* cum = p.meta;
   const int* nlen = p.meta + p.B + 1;
@@ -445,63 +337,91 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
     const int g = bg % p.Hkv, b = bg / p.Hkv;
     const int n = nlen[b];
     if (n < 0) return;
+    const int G = p.G;
     const int64_t base = p.seq_offset[b];
     const __nv_bfloat16* kn = p.k_new ? p.k_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
                                       : p.K + ((base + n) * p.Hkv + g) * D;
     const __nv_bfloat16* vn = p.v_new ? p.v_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
                                       : p.V + ((base + n) * p.Hkv + g) * D;
     const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
-    const int npairs = p.G * (t + 1);
-    for (int pr = warp; pr < npairs; pr += 4) {
+    // segments of this (sequence, KV head)
+    const int tiles = cum[b + 1] - cum[b];
+    const int64_t T = static_cast<int64_t>(p.Hkv) * cum[p.B];
+    int64_t cf = 0, cl = -1;
+    if (tiles > 0) {
+      const int64_t S = static_cast<int64_t>(p.Hkv) * cum[b] + static_cast<int64_t>(g) * tiles;
+      cf = owner_cta(S, T, p.nctas);
+      cl = owner_cta(S + tiles - 1, T, p.nctas);
+    }
+    const int nseg = static_cast<int>(cl - cf + 1);
+    const size_t pair = static_cast<size_t>(b) * p.Hkv + g;
+    float* cm = cs;
+    float* csum = cs + p.nctas * G;
+    // phase 1: one round of independent loads into shared memory
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    const __nv_bfloat16* qbase = p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G) * D;
+    for (int e = tid; e < G * CH; e += 128)
+      reinterpret_cast<uint4*>(&qs[0][0])[e] = reinterpret_cast<const uint4*>(qbase)[e];
+    for (int e = tid; e < (t + 1) * CH; e += 128) {
+      const int u = e / CH, c = e - u * CH;
+      reinterpret_cast<uint4*>(&ks[u][0])[c] = reinterpret_cast<const uint4*>(kn + u * row_stride)[c];
+      reinterpret_cast<uint4*>(&vs[u][0])[c] = reinterpret_cast<const uint4*>(vn + u * row_stride)[c];
+    }
+    for (int e = tid; e < nseg * G; e += 128) {
+      const int si = e / G, jh = e - si * G;
+      const int64_t c = cf + si;
+      float ms = NEG, ls = 0.f;
+      if (split_nonempty(c, T, p.nctas)) {  // CTAs with no items wrote no partial
+        const size_t r = (static_cast<size_t>(c) + pair) * p.Mpad + t * G + jh;
+        ms = p.part_ml[r * 2 + 0];
+        ls = p.part_ml[r * 2 + 1];
+      }
+      cm[si * G + jh] = ms;
+      csum[si * G + jh] = ls;
+    }
+    __syncthreads();
+    // logits of the verify rows' own keys u <= t (causal), from shared memory
+    for (int pr = warp; pr < G * (t + 1); pr += 4) {
       const int jh = pr / (t + 1), u = pr - jh * (t + 1);
-      const __nv_bfloat16* qr = p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * p.G + jh) * D;
-      const __nv_bfloat16* kr = kn + u * row_stride;
       float acc = 0.f;
-      for (int e = lane; e < D; e += 32) acc += bf2f(qr[e]) * bf2f(kr[e]);
+      for (int e = lane; e < D; e += 32) acc += bf2f(qs[jh][e]) * bf2f(ks[u][e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (lane == 0) lg[jh][u] = acc * p.scale_log2;
     }
     __syncthreads();
-    const int tiles = cum[b + 1] - cum[b];
-    int64_t cf = 0, cl = -1;
-    if (tiles > 0) {
-      const int64_t T = static_cast<int64_t>(p.Hkv) * cum[p.B];
-      const int64_t S = static_cast<int64_t>(p.Hkv) * cum[b] + static_cast<int64_t>(g) * tiles;
-      cf = owner_cta(S, T, p.nctas);
-      cl = owner_cta(S + tiles - 1, T, p.nctas);
-    }
-    const size_t pair = static_cast<size_t>(b) * p.Hkv + g;
-    if (tid < D) {
-      const int e = tid;
-      for (int jh = 0; jh < p.G; ++jh) {
-        const int m = t * p.G + jh;
-        float M = NEG, acc = 0.f, l = 0.f;
-        for (int64_t c = cf; c <= cl; ++c) {
-          const size_t id = static_cast<size_t>(c) + pair;
-          const float ms = p.part_ml[(id * p.Mpad + m) * 2 + 0];
-          const float ls = p.part_ml[(id * p.Mpad + m) * 2 + 1];
-          const float os = p.part_o[(id * p.Mpad + m) * D + e];
-          const float Mn = fmaxf(M, ms);
-          const float a = ex2(M - Mn), w = ex2(ms - Mn);
-          acc = acc * a + os * w;
-          l = l * a + ls * w;
-          M = Mn;
-        }
-        for (int u = 0; u <= t; ++u) {
-          const float lu = lg[jh][u];
-          const float Mn = fmaxf(M, lu);
-          const float a = ex2(M - Mn), w = ex2(lu - Mn);
-          acc = acc * a + w * bf2f(vn[u * row_stride + e]);
-          l = l * a + w;
-          M = Mn;
-        }
-        p.out[((static_cast<size_t>(b) * p.R + t) * p.Hq + g * p.G + jh) * D + e] = __float2bfloat16_rn(acc / l);
+    // phase 2: one warp per query row, lanes across d
+    constexpr int PER = D / 32;
+    for (int jh = warp; jh < G; jh += 4) {
+      float M = NEG;
+      for (int si = lane; si < nseg; si += 32) M = fmaxf(M, cm[si * G + jh]);
+      for (int u = lane; u <= t; u += 32) M = fmaxf(M, lg[jh][u]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float acc[PER];
+#pragma unroll
+      for (int q = 0; q < PER; ++q) acc[q] = 0.f;
+      float l = 0.f;
+      const int m = t * G + jh;
+      merge_partials<D>(cm + jh, csum + jh, G, nseg, M,
+                        [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + m) * D; },
+                        acc, l, lane);
+      for (int u = 0; u <= t; ++u) {
+        const float w = ex2(lg[jh][u] - M);
+        l += w;
+#pragma unroll
+        for (int q = 0; q < PER; ++q) acc[q] += w * bf2f(vs[u][lane * PER + q]);
       }
-      if (p.k_new) {  // append verify row t (Vegas §2 step 1: the chain enters the cache)
-        const size_t dst = ((base + n + t) * p.Hkv + g) * D + e;
-        p.K[dst] = kn[t * row_stride + e];
-        p.V[dst] = vn[t * row_stride + e];
+      const float inv = 1.f / l;
+      __nv_bfloat16* o = p.out + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + lane * PER;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) o[q] = __float2bfloat16_rn(acc[q] * inv);
+    }
+    if (p.k_new) {  // append verify row t (the chain enters the cache)
+      const size_t dst = ((base + n + t) * p.Hkv + g) * D;
+      for (int c = tid; c < CH; c += 128) {
+        reinterpret_cast<uint4*>(p.K + dst)[c] = reinterpret_cast<const uint4*>(&ks[t][0])[c];
+        reinterpret_cast<uint4*>(p.V + dst)[c] = reinterpret_cast<const uint4*>(&vs[t][0])[c];
       }
     }
     return;
@@ -516,10 +436,12 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
   for (int ms = 0; ms < 2; ++ms) {
     float* dst = ms ? p.scores1 : p.scores0;
     if ((ms ? p.mask1 : p.mask0) == 0u || dst == nullptr) continue;
-    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * p.Hkv * p.max_len;
+    const int parts = p.Hkv * (p.Mpad / 16);  // (KV head, m-tile) shares, in a fixed order
+    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.max_len;
     for (int pos = lo + tid; pos < hi; pos += 128) {
       float v = 0.f;
-      for (int g = 0; g < p.Hkv; ++g) v += src[static_cast<size_t>(g) * p.max_len + pos];
+#pragma unroll 8
+      for (int q = 0; q < parts; ++q) v += src[static_cast<size_t>(q) * p.max_len + pos];
       dst[static_cast<size_t>(b) * p.score_stride + pos] = v;
     }
   }
@@ -530,19 +452,27 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
                             cudaStream_t stream) {
   using C = VCfg<D, MT>;
   const size_t smem = C::smem(p.B);
-  cudaError_t e = cudaFuncSetAttribute(verify_kernel<D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem<verify_kernel<D, MT>>(smem);
   if (e != cudaSuccess) return e;
   verify_kernel<D, MT><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, verify_kernel<D, MT>) == cudaSuccess) {
+      fprintf(stderr,
+              "verify_kernel<%d,%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
+              "requestedSmem=%zu localBytes=%zu)\n",
+              D, MT, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, C::THREADS, fa.sharedSizeBytes,
+              fa.maxDynamicSharedSizeBytes, smem, fa.localSizeBytes);
+    }
+    return e;
+  }
   const int nO = p.B * p.Hkv * p.R;
   const int nS = ((p.mask0 | p.mask1) != 0u) ? p.B * ((p.max_len + kScoreChunk - 1) / kScoreChunk) : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nO + nS);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.nctas) * p.G * 2 * sizeof(float);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

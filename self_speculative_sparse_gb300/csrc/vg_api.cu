@@ -170,7 +170,7 @@ WsLayout ws_layout(const Shape& s, int sms) {
   w.part_ml = off;
   off = up256(off + segs * s.Mpad * 2 * 4);
   w.part_s = off;
-  off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * static_cast<size_t>(s.max_len) * 4);
+  off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * (s.Mpad / 16) * static_cast<size_t>(s.max_len) * 4);
   const size_t verify_total = off;
   const size_t dsegs = static_cast<size_t>(sms) + s.B;
   off = 0;  // the draft step's scratch reuses the same bytes (calls are stream-ordered)
@@ -286,7 +286,9 @@ vg_status check_topk_args(const float* scores, int64_t stride, const int32_t* le
 
 vg_status run_topk(const float* scores, int64_t stride, const int32_t* len, int B, int max_len, int k, int32_t* idx,
                    int32_t* count, int32_t* dev_status, cudaStream_t stream, bool pdl) {
-  int C = (max_len + 16383) / 16384;
+  // one CTA per 4096 positions, up to a cluster of 8: the radix passes are
+  // latency-bound, so shorter slices per CTA finish sooner
+  int C = (max_len + 4095) / 4096;
   C = C < 1 ? 1 : (C > 8 ? 8 : C);
   int per = (max_len + C - 1) / C;
   per = ((per + 3) / 4) * 4;
@@ -330,9 +332,9 @@ vg_status check_draft_args(const DraftArgs& a) {
 
 vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, void* ws, const WsLayout& w,
                     const DevInfo& di, int32_t* dev_status, cudaStream_t stream, bool pdl) {
-  const int stages = draft_stages(s.Hkv, s.D);
-  if (draft_smem_bytes(s.Hkv, s.D, stages, s.B) > di.smem_optin)
-    return fail(VG_ERR_UNSUPPORTED_SHAPE, "draft needs too much shared memory");
+  if (draft_smem_bytes(s.D, s.Hkv, s.B) > di.smem_optin)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d needs more shared memory than a CTA has",
+                s.Hkv * s.D);
   DraftParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
@@ -355,7 +357,6 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.nctas = di.sms;
-  p.stages = stages;
   p.meta = at<int32_t>(ws, w.dmeta);
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);

@@ -82,6 +82,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// Orders this thread's earlier generic-proxy shared-memory accesses before its later
+// async-proxy (TMA / bulk copy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -92,6 +97,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 16-byte global -> shared copy (LDGSTS); src_bytes = 0 zero-fills the destination.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on bar once all of this thread's earlier cp.async copies have landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // ------------------------------------------------------------------ tensor cores
@@ -127,6 +143,13 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // ------------------------------------------------------------------ sync
+// Shared-memory counter increment with acquire-release semantics at CTA scope:
+// the warp that sees the last arrival also sees every earlier arriver's accesses.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_smem(uint32_t* addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(addr)), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -143,5 +166,25 @@ __host__ __device__ __forceinline__ int64_t owner_cta(int64_t x, int64_t T, int6
   return ((x + 1) * N - 1) / T;
 }
 __host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t T, int64_t N) { return (c * T) / N; }
+// True if CTA c of that split owns at least one item (with T < N some own none).
+__host__ __device__ __forceinline__ bool split_nonempty(int64_t c, int64_t T, int64_t N) {
+  return split_begin(c, T, N) < split_begin(c + 1, T, N);
+}
+
+// Sets a kernel's dynamic shared-memory limit once per device (and again only if a
+// larger size is asked for), so repeated launches - and launches under stream
+// capture - make no attribute calls.
+template <auto Kernel>
+inline cudaError_t ensure_smem(size_t bytes) {
+  static int done[64] = {0};  // one table per kernel (the template argument is the kernel itself)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev] >= static_cast<int>(bytes)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done[dev] = static_cast<int>(bytes);
+  return e;
+}
 
 }  // namespace vg

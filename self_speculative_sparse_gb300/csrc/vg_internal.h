@@ -14,8 +14,8 @@ namespace vg {
 constexpr int kVerifyTileKeys = 64;
 // Prefix positions per score-reduction block of the verify combine kernel.
 constexpr int kScoreChunk = 1024;
-// Positions per pipeline stage of the sparse draft kernel.
-constexpr int kDraftStageKeys = 16;
+// Longest draft-token tail a sparse draft step attends besides the selection.
+constexpr int kDraftMaxTail = 64;
 // Largest sequence the top-k kernel holds in shared memory across a cluster of 8.
 constexpr int kTopkMaxLen = 262144;
 constexpr int kMaxBatch = 1024;
@@ -39,7 +39,7 @@ struct VerifyParams {
   int32_t* meta;     // [B + 1] tiles-per-head prefix sums, then [B] checked lengths
   float* part_o;     // [nctas + B*Hkv][Mpad][D]  unnormalised partial outputs
   float* part_ml;    // [nctas + B*Hkv][Mpad][2]  (running max in log2 units, sum)
-  float* part_s;     // [2][B][Hkv][max_len]       per-KV-head partial scores
+  float* part_s;     // [2][B][Hkv][Mpad/16][max_len]  per-(KV head, m-tile) partial scores
   // outputs
   float* scores0;    // [B][score_stride] or null
   float* scores1;
@@ -76,9 +76,8 @@ struct DraftParams {
   int B, Hq, Hkv, G, D;
   float scale, scale_log2;
   int nctas;
-  int stages;
   int32_t* meta;               // [B + 1] entry prefix sums
-  float* part_o;               // [nctas + B][Hq][D]
+  float* part_o;               // [nctas + B][Hq][D]  unnormalised partial outputs
   float* part_ml;              // [nctas + B][Hq][2]
   __nv_bfloat16* out;          // [B][Hq][D]
   int32_t* status;
@@ -91,7 +90,6 @@ size_t verify_smem_bytes(int D, int Mpad, int B);
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
 size_t topk_smem_bytes(int per_cta);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
-int draft_stages(int Hkv, int D);
-size_t draft_smem_bytes(int Hkv, int D, int stages, int B);
+size_t draft_smem_bytes(int D, int Hkv, int B);
 
 }  // namespace vg

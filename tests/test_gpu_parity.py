@@ -48,6 +48,7 @@ def test_iteration_matches_oracle(name):
     w = CASES[name]
     pool = w.layer_pool(0)
     st = LayerState(w, pool)
+    st.ws.fill_(0x7F)             # garbage workspace: results must not depend on its contents
     st.iteration()
     torch.cuda.synchronize()
     assert st.check_status() == 0, f"device status {st.check_status()}"
