@@ -345,9 +345,9 @@ def run_ours(args, rank, local, world):
     t_verify = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
     t_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
     t_draft = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
-    for st in states:
-        if st.check_status() != 0:
-            raise RuntimeError(f"device status {st.check_status()}")
+    bad = [(i, st.check_status()) for i, st in enumerate(states) if st.check_status() != 0]
+    if bad:
+        raise RuntimeError(f"device status (copy, code): {bad}")
 
     # ---- end to end through the public C ABI (vg_iteration) with host buffers
     e2e_steps = args.e2e_steps or args.steps

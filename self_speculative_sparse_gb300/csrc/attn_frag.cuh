@@ -67,6 +67,24 @@ __device__ __forceinline__ void qk16(const uint32_t (&qf)[D / 16][4], KAddr kadd
     for (int c = 0; c < 4; ++c) s[nt][c] += t[nt][c];
 }
 
+// Column sums of a 16x16 S tile over the warp's 16 rows, in 4 shuffles: v[nt*2+c]
+// holds this thread's (row-masked) contribution to key nt*8 + tig*2 + c.  A
+// transposing butterfly halves the values carried at each step; the result is the
+// sum for key ((lane >> 4) & 1) * 8 + tig * 2 + ((lane >> 3) & 1), and lanes that
+// differ only in bit 2 hold the same sum.
+__device__ __forceinline__ float colsum16(const float (&v)[4], int lane) {
+  const bool h2 = (lane & 16) != 0;
+  float k0 = h2 ? v[2] : v[0];
+  float k1 = h2 ? v[3] : v[1];
+  k0 += __shfl_xor_sync(0xffffffffu, h2 ? v[0] : v[2], 16);
+  k1 += __shfl_xor_sync(0xffffffffu, h2 ? v[1] : v[3], 16);
+  const bool h1 = (lane & 8) != 0;
+  float keep = h1 ? k1 : k0;
+  keep += __shfl_xor_sync(0xffffffffu, h1 ? k0 : k1, 8);
+  keep += __shfl_xor_sync(0xffffffffu, keep, 4);
+  return keep;
+}
+
 // Online-softmax update with 16 logits per row already in log2 units (masked
 // keys at -inf), then O += P V.  vaddr(r, c16) as kaddr, for the value rows.
 template <int D, typename VAddr>
@@ -195,6 +213,53 @@ __device__ __forceinline__ void store_partial(const float* merge, int ms, const 
     out_ml[r * 2 + 1] = lrow[r];
   }
 }
+
+// Register prefetch of up to NB partial output rows for one warp (partials first,
+// first + step, ...): the loads are issued before their weights are known, so they
+// overlap the loads of the maxima and sums.  Out-of-range slots read partial
+// `first` again (a readable address) and are never used.
+template <int D, int NB>
+struct PartialRows {
+  float v[NB][D / 32];
+  template <typename ORow>
+  __device__ __forceinline__ void load(ORow orow, int first, int step, int nseg, int lane) {
+    constexpr int PER = D / 32;
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int si = first + q * step < nseg ? first + q * step : first;
+      const float* src = orow(si) + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(src);
+        v[q][0] = t.x;
+        v[q][1] = t.y;
+        v[q][2] = t.z;
+        v[q][3] = t.w;
+      } else {
+        const float2 t = *reinterpret_cast<const float2*>(src);
+        v[q][0] = t.x;
+        v[q][1] = t.y;
+      }
+    }
+  }
+  // acc += sum w_s O_s, l += sum w_s l_s over the prefetched partials
+  __device__ __forceinline__ void accumulate(const float* cm, const float* csum, int cstride, int first, int step,
+                                             int nseg, float M, float (&acc)[D / 32], float& l) const {
+    const float NEG = neg_inf();
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int si = first + q * step;
+      if (si < nseg) {
+        const float ms = cm[si * cstride];
+        if (ms != NEG) {
+          const float w = ex2(ms - M);
+          l += w * csum[si * cstride];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) acc[c] += w * v[q][c];
+        }
+      }
+    }
+  }
+};
 
 // One warp merges the partials of one query row: acc[lane's d values] and l get
 // sum_s w_s * O_s and sum_s w_s * l_s with w_s = 2^(m_s - M).  Partial s has its

@@ -7,8 +7,11 @@
 //
 // GB300 design.  A token's page is its cache slot: all KV heads contiguous, H_kv*d*2
 // bytes of K and as many of V.  Each sequence's attended entries are its selected
-// positions followed by the tail of draft-token slots; the flattened list of
-// (sequence, entry) items is split evenly over one persistent CTA per SM.  A
+// positions followed by the tail of draft-token slots.  The work is the fixed grid
+// of (sequence, entry slot) items, k_stride + a tail bound slots per sequence (slots
+// past the sequence's entries are masked), split evenly over one persistent CTA per
+// SM: the split needs no device data, so each CTA's first memory round trip already
+// fetches its positions, and the combine kernel knows where the partials are.  A
 // producer warp turns each entry into two TMA bulk copies of a whole page (large
 // requests keep the copy engine efficient; the current draft token comes straight
 // from the inputs) landing in a padded, bank-conflict-free shared-memory ring
@@ -30,15 +33,14 @@ constexpr int kCombineWarps = 8;
 
 struct DLayout {
   int row;  // bytes per gathered page in shared memory (padded by 16: ldmatrix rows hit distinct banks)
-  int half, stage, off_pos, off_bar, off_cum, total;
-  __host__ __device__ DLayout(int Hkv, int D, int B) {
+  int half, stage, off_pos, off_bar, total;
+  __host__ __device__ DLayout(int Hkv, int D) {
     row = Hkv * D * 2 + 16;
     half = kKeys * row;
     stage = 2 * half;
     off_pos = kStages * stage;                           // int [kStages][kKeys]
     off_bar = (off_pos + kStages * kKeys * 4 + 7) & ~7;  // full[kStages], empty[kStages]
-    off_cum = off_bar + 2 * kStages * 8;                 // int cum[B + 1], cnt[B]
-    total = off_cum + (2 * B + 1) * 4;
+    total = off_bar + 2 * kStages * 8;
   }
 };
 
@@ -46,51 +48,9 @@ __device__ __forceinline__ int tail_len_of(const DraftParams& p, int b) {
   return p.tail_len ? p.tail_len[b] : p.tail_len_const;
 }
 
-// Attended entries per sequence - the selected ones, then the draft-token tail -
-// checked, with their prefix sums (cum) and selected counts (cnt); warp 0 only.
-__device__ void draft_meta(const DraftParams& p, int* cum, int* cnt) {
-  const int lane = threadIdx.x & 31;
-  int carry = 0;
-  for (int b0 = 0; b0 < p.B; b0 += 32) {
-    const int b = b0 + lane;
-    int e = 0;
-    if (b < p.B) {
-      const int c = p.count[b];
-      const int tl = tail_len_of(p, b);
-      const int64_t off = p.seq_offset[b];
-      const int ts = p.tail_start[b];
-      const bool ok = c >= 0 && c <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && off >= 0 && ts >= 0 &&
-                      off + ts + tl <= p.capacity && (p.k_new == nullptr || tl >= 1);
-      if (!ok) report(p.status, VG_ERR_DEVICE_BOUNDS);
-      cnt[b] = ok ? c : 0;
-      e = ok ? c + tl : 0;
-    }
-    int v = e;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
-    }
-    if (b < p.B) cum[b] = carry + v - e;
-    carry += __shfl_sync(0xffffffffu, v, 31);
-  }
-  if (lane == 0) cum[p.B] = carry;
-}
-
-// Item x -> (sequence b, entry j within it).
-__device__ __forceinline__ void locate(int x, const int* cum, int B, int& b, int& j) {
-  int lo = 0, hi = B;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  b = lo;
-  j = x - cum[b];
-}
-
-__device__ __forceinline__ void next_seq(int& b, const int* cum, int B) {
-  ++b;
-  while (b < B && cum[b + 1] == cum[b]) ++b;
+// Entry slots per sequence in the static work split.
+__host__ __device__ __forceinline__ int draft_slots(const DraftParams& p) {
+  return p.k_stride + (p.tail_len ? kDraftMaxTail : p.tail_len_const);
 }
 
 // MAXW: the most KV heads (consumer warps) this instantiation serves.
@@ -98,18 +58,14 @@ template <int D, int MAXW>
 __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const DLayout L(p.Hkv, D, p.B);
+  const DLayout L(p.Hkv, D);
   int* posb = reinterpret_cast<int*>(smem + L.off_pos);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
   uint64_t* empty = full + kStages;
-  int* cum = reinterpret_cast<int*>(smem + L.off_cum);
-  int* cnt = cum + p.B + 1;
   const int W = p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float NEG = neg_inf();
 
-  pdl_wait();  // idx / count come from the selection kernel
-  if (warp == 0) draft_meta(p, cum, cnt);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -118,43 +74,46 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     fence_mbar_init();
   }
   __syncthreads();
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < p.B + 1; i += blockDim.x) p.meta[i] = cum[i];
-  }
-  pdl_launch_dependents();
-
-  const int E = cum[p.B];
+  const int S = draft_slots(p);
+  const int64_t E = static_cast<int64_t>(p.B) * S;
   const int x0 = static_cast<int>(split_begin(blockIdx.x, E, p.nctas));
   const int x1 = static_cast<int>(split_begin(blockIdx.x + 1, E, p.nctas));
+  pdl_launch_dependents();
   if (x0 >= x1) return;
+  pdl_wait();  // idx / count come from the selection kernel
   const int page = p.Hkv * D * 2;  // bytes of one token's K (or V), all heads
 
   // ------------------------------------------------------------ producer warp
   if (warp == W) {
-    int b, j;
-    locate(x0, cum, p.B, b, j);
+    int b = x0 / S, j = x0 - b * S;
     int stage = 0;
     uint32_t phase = 0;
     for (int x = x0; x < x1;) {
-      const int nvalid = min(kKeys, min(x1 - x, (cum[b + 1] - cum[b]) - j));
+      const int nvalid = min(kKeys, min(x1 - x, S - j));
       bool ok_wait = true;
       if (lane == 0) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
       if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
-      const int ts = p.tail_start[b];
-      const int nsel = cnt[b];
+      // one round of independent loads: this sequence's counts and the chunk's positions
+      const int jj = j + lane;  // selected entries first, then the draft-token tail
+      const int cnt_raw = p.count[b];
       const int tl = tail_len_of(p, b);
+      const int ts = p.tail_start[b];
       const int64_t off = p.seq_offset[b];
+      const int sel = (lane < nvalid && jj < p.k_stride) ? p.idx[static_cast<size_t>(b) * p.k_stride + jj] : 0;
+      const bool seq_ok = cnt_raw >= 0 && cnt_raw <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && off >= 0 &&
+                          ts >= 0 && off + ts + tl <= p.capacity && (p.k_new == nullptr || tl >= 1);
+      if (!seq_ok && lane == 0 && j == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
+      const int nsel = seq_ok ? cnt_raw : 0;
       uint8_t* kst = smem + stage * L.stage;
       int pos = -1;
-      if (lane < nvalid) {
-        const int jj = j + lane;  // selected entries first, then the draft-token tail
+      if (seq_ok && lane < nvalid) {
         if (jj < nsel) {
-          pos = p.idx[static_cast<size_t>(b) * p.k_stride + jj];
+          pos = sel;
           if (pos < 0 || pos >= ts) {
             report(p.status, VG_ERR_DEVICE_BOUNDS);
             pos = -1;
           }
-        } else {
+        } else if (jj < nsel + tl) {
           pos = ts + (jj - nsel);
         }
       }
@@ -185,9 +144,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
       }
       x += nvalid;
       j += nvalid;
-      if (x < x1 && j == cum[b + 1] - cum[b]) {
+      if (j == S) {
         j = 0;
-        next_seq(b, cum, p.B);
+        ++b;
       }
       if (++stage == kStages) {
         stage = 0;
@@ -200,13 +159,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   // ------------------------------------------------------------ consumer warp: KV head g
   const int g = warp;
   const int gid = lane >> 2, tig = lane & 3;
-  int b, j;
-  locate(x0, cum, p.B, b, j);
+  int b = x0 / S, j = x0 - b * S;
   int stage = 0;
   uint32_t phase = 0;
   bool lost = false;
   for (int x = x0; x < x1 && !lost;) {
-    const int seg_end = min(x1, x + (cum[b + 1] - cum[b]) - j);
+    const int seg_end = min(x1, x + (S - j));
     uint32_t qf[D / 16][4];
     load_q_frags<D>(qf, gid < p.G ? p.q + (static_cast<size_t>(b) * p.Hq + g * p.G + gid) * D : nullptr,
                     gid + 8 < p.G ? p.q + (static_cast<size_t>(b) * p.Hq + g * p.G + gid + 8) * D : nullptr, tig);
@@ -268,7 +226,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     }
     if (x < x1) {
       j = 0;
-      next_seq(b, cum, p.B);
+      ++b;
     }
   }
 }
@@ -283,22 +241,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) draft_combine_kernel(const
   __shared__ float red[kCombineWarps][D];
   __shared__ float redl[kCombineWarps];
   __shared__ float redm[kCombineWarps];
-  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG = neg_inf();
-  const int* cum = p.meta;
-  const int Eb = cum[b + 1] - cum[b];
-  const int64_t E = cum[p.B];
-  int64_t cf = 0, cl = -1;
-  if (Eb > 0) {
-    cf = owner_cta(cum[b], E, p.nctas);
-    cl = owner_cta(cum[b] + Eb - 1, E, p.nctas);
-  }
+  // the partials of sequence b come from the CTAs whose static ranges meet its slots
+  const int S = draft_slots(p);
+  const int64_t E = static_cast<int64_t>(p.B) * S;
+  const int64_t cf = owner_cta(static_cast<int64_t>(b) * S, E, p.nctas);
+  const int64_t cl = owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, p.nctas);
   const int nseg = static_cast<int>(cl - cf + 1);
+  pdl_wait();
   float* cm = cs;
   float* csum = cs + p.nctas;
+  // each warp's share of the partial output rows goes to registers first, so these
+  // loads overlap those of the maxima and sums
+  constexpr int NB = 16;
+  auto orow = [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + b) * p.Hq + h) * D; };
+  PartialRows<D, NB> pre;
+  pre.load(orow, warp, kCombineWarps, nseg, lane);
   for (int si = tid; si < nseg; si += kCombineWarps * 32) {
     const int64_t c = cf + si;
     float ms = NEG, ls = 0.f;
@@ -325,9 +286,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) draft_combine_kernel(const
 #pragma unroll
   for (int q = 0; q < PER; ++q) acc[q] = 0.f;
   float l = 0.f;
-  merge_partials<D>(cm, csum, 1, nseg, M,
-                    [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + b) * p.Hq + h) * D; }, acc, l,
-                    lane, warp, kCombineWarps);
+  pre.accumulate(cm, csum, 1, warp, kCombineWarps, nseg, M, acc, l);
+  merge_partials<D>(cm, csum, 1, nseg, M, orow, acc, l, lane, warp + NB * kCombineWarps, kCombineWarps);
 #pragma unroll
   for (int q = 0; q < PER; ++q) red[warp][lane * PER + q] = acc[q];
   if (lane == 0) redl[warp] = l;
@@ -358,7 +318,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) draft_combine_kernel(const
 
 template <int D, int MAXW>
 cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) {
-  const size_t smem = static_cast<size_t>(DLayout(p.Hkv, D, p.B).total) + 128;
+  const size_t smem = static_cast<size_t>(DLayout(p.Hkv, D).total) + 128;
   cudaError_t e = ensure_smem<draft_kernel<D, MAXW>>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
@@ -385,7 +345,7 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
 
 }  // namespace
 
-size_t draft_smem_bytes(int D, int Hkv, int B) { return static_cast<size_t>(DLayout(Hkv, D, B).total) + 128; }
+size_t draft_smem_bytes(int D, int Hkv) { return static_cast<size_t>(DLayout(Hkv, D).total) + 128; }
 
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl) {
   if (p.Hkv <= 8) {

@@ -10,8 +10,10 @@
 // keeps its contiguous slice of the scores in shared memory as order-preserving
 // 32-bit keys.  An exact MSB-first radix select (4 passes of 8 bits) finds the
 // k-th largest key: every pass builds per-warp histograms with warp-aggregated
-// increments (no same-bin atomic conflicts), the cluster sums them through
-// distributed shared memory, and every CTA picks the same digit.  A final
+// increments (one atomic per distinct digit per warp step, eight steps in flight,
+// no contention between warps), the cluster sums them through distributed shared
+// memory, and a block-wide scan over the digits lets every CTA pick the same
+// digit.  A final
 // cluster-wide exclusive scan in position order writes the selected positions,
 // taking the needed number of threshold-equal keys from the lowest positions.
 // Everything is integer work: the result is bit-exact and deterministic.
@@ -27,6 +29,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBins = 256;  // radix digit: 8 bits
 
 // fp32 -> key with the same order; -0.0 is mapped to the key of +0.0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -38,12 +41,11 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t tk_smem[];
   uint32_t* keys = tk_smem;                          // [per_cta]
-  uint32_t* hist = keys + p.per_cta;                 // [2][kWarps][256] per-warp histograms
-  uint32_t* hsum = hist + 2 * kWarps * 256;          // [2][256]
-  int* wsum = reinterpret_cast<int*>(hsum + 2 * 256);  // [32]
+  uint32_t* hist = keys + p.per_cta;                 // [kWarps][kBins] per-warp digit histograms
+  uint32_t* hsum = hist + kWarps * kBins;            // [2][kBins] CTA histograms (double-buffered)
+  int* wsum = reinterpret_cast<int*>(hsum + 2 * kBins);  // [32]
   int* misc = wsum + 32;                             // [48]
   int* cnts = misc + 48;                             // [2]: this CTA's (#greater, #equal)
-  uint32_t* revc = reinterpret_cast<uint32_t*>(cnts + 2);  // [256] digit counts, highest first
 
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
@@ -117,76 +119,89 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     }
   }
 
+  __syncthreads();  // the passes read keys that other threads stored
+
   // ---------------------------------------------------------------- radix select
   uint32_t prefix = 0u, pmask = 0u;
   int remaining = cnt;  // how many keys >= the threshold are still to be taken inside the prefix class
+  const int rounds = (mine + kThreads - 1) / kThreads;
+#pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    const int hb = pass & 1;
-    uint32_t* h = hist + hb * kWarps * 256;
-    for (int i = tid; i < kWarps * 256; i += kThreads) h[i] = 0u;
-    __syncthreads();
-    // warp-aggregated counting: lanes with the same digit add once, into their
-    // warp's own histogram, so concentrated digits cause no atomic conflicts
-    uint32_t* hw = h + (tid >> 5) * 256;
-    const int rounds = (mine + kThreads - 1) / kThreads;
-    for (int rd = 0; rd < rounds; ++rd) {
-      const int i = rd * kThreads + tid;
-      const uint32_t key = i < mine ? keys[i] : 0u;
-      const bool cand = i < mine && (key & pmask) == prefix;
-      const uint32_t dg = cand ? ((key >> shift) & 255u) : 256u;
-      const unsigned peers = __match_any_sync(0xffffffffu, dg);
-      if (cand && lane == __ffs(peers) - 1) atomicAdd(&hw[dg], static_cast<uint32_t>(__popc(peers)));
+    uint32_t* hw = hist + (tid >> 5) * kBins;
+    for (int i = lane; i < kBins; i += 32) hw[i] = 0u;  // this warp's own histogram
+    __syncwarp();
+    // warp-aggregated counting, eight independent steps at a time: lanes with the
+    // same digit add once, into their warp's histogram
+    for (int rb = 0; rb < rounds; rb += 8) {
+      uint32_t dg[8];
+      bool cand[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = (rb + q) * kThreads + tid;
+        const bool in = i < mine;
+        const uint32_t key = in ? keys[i] : 0u;
+        cand[q] = in && (key & pmask) == prefix;
+        dg[q] = cand[q] ? ((key >> shift) & 255u) : 0xffffffffu;
+      }
+      unsigned peers[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) peers[q] = __match_any_sync(0xffffffffu, dg[q]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (cand[q] && lane == __ffs(peers[q]) - 1) atomicAdd(&hw[dg[q]], static_cast<uint32_t>(__popc(peers[q])));
     }
     __syncthreads();
-    if (tid < 256) {
-      uint32_t s = 0;
+    uint32_t* h = hsum + (pass & 1) * kBins;
+    if (tid < kBins) {
+      uint32_t sum = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += h[w * 256 + tid];
-      hsum[hb * 256 + tid] = s;
+      for (int w = 0; w < kWarps; ++w) sum += hist[w * kBins + tid];
+      h[tid] = sum;
     }
     cluster.sync();
-    // cluster-wide count of each digit, stored highest digit first
-    if (tid < 256) {
-      uint32_t tot = 0;
-      for (int rr = 0; rr < C; ++rr) tot += *cluster.map_shared_rank(&hsum[hb * 256 + tid], rr);
-      revc[255 - tid] = tot;
+    // cluster-wide counts, highest digit first: thread t (< 256) owns digit 255 - t
+    int c4[1];
+    int tsum = 0;
+    {
+      int c = 0;
+      if (tid < kBins) {
+        uint32_t* hd = &h[kBins - 1 - tid];
+        for (int rr = 0; rr < C; ++rr) c += static_cast<int>(*cluster.map_shared_rank(hd, rr));
+      }
+      c4[0] = c;
+      tsum = c;
+    }
+    // block-wide exclusive scan of the per-thread sums (in descending digit order)
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[tid >> 5] = incl;
+    __syncthreads();
+    if (tid < 32) {
+      const int wv = tid < kWarps ? wsum[tid] : 0;
+      int wi = wv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      if (tid < kWarps) wsum[tid] = wi - wv;
     }
     __syncthreads();
-    // warp 0 walks the digits from the top, 32 at a time, to the one holding the
-    // remaining-th largest key of the current prefix class
-    if (tid < 32) {
-      int above = 0, found = -1, found_above = 0;
-      for (int base = 0; base < 256 && found < 0; base += 32) {
-        const int c = static_cast<int>(revc[base + lane]);  // digit 255 - (base + lane)
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const int excl = above + incl - c;  // keys of this class in higher digits
-        const bool hit = excl < remaining && remaining <= excl + c;
-        const unsigned ball = __ballot_sync(0xffffffffu, hit);
-        if (ball) {
-          const int src_lane = __ffs(ball) - 1;
-          found = 255 - (base + src_lane);
-          found_above = __shfl_sync(0xffffffffu, excl, src_lane);
-        }
-        above += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) {
-        misc[0] = found;
-        misc[1] = found_above;
-      }
+    // the digit whose keys hold the remaining-th largest of the prefix class
+    const int run = wsum[tid >> 5] + incl - tsum;
+    if (tid < kBins && run < remaining && remaining <= run + c4[0]) {
+      misc[0] = kBins - 1 - tid;
+      misc[1] = run;
     }
     __syncthreads();
     const int digit = misc[0];
-    if (digit < 0) {  // cannot happen with consistent counts; stay safe
-      report(p.status, VG_ERR_DEVICE_BOUNDS);
-    }
     remaining -= misc[1];
-    prefix |= static_cast<uint32_t>(digit & 255) << shift;
+    prefix |= static_cast<uint32_t>(digit) << shift;
     pmask |= 255u << shift;
     __syncthreads();
   }
@@ -261,7 +276,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     const unsigned eqm = __ballot_sync(0xffffffffu, eq);
     const bool sel = gt || (eq && eq_rank + __popc(eqm & lt) < take_mine);
     const unsigned selm = __ballot_sync(0xffffffffu, sel);
-    if (sel) out[sel_base + __popc(selm & lt)] = start + i;
+    const int slot = sel_base + __popc(selm & lt);
+    if (sel && slot < cnt) out[slot] = start + i;  // (slot < cnt always holds for consistent counts)
     sel_base += __popc(selm);
     eq_rank += __popc(eqm);
   }
@@ -270,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 }  // namespace
 
 size_t topk_smem_bytes(int per_cta) {
-  return static_cast<size_t>(per_cta) * 4 + (2 * kWarps * 256 + 2 * 256) * 4 + (32 + 48 + 2 + 256) * 4;
+  return static_cast<size_t>(per_cta) * 4 + (kWarps + 2) * kBins * 4 + (32 + 48 + 2) * 4;
 }
 
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl) {

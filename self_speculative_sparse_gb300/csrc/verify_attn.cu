@@ -47,9 +47,8 @@ struct VCfg {
   static constexpr int OFF_MERGE = kStages * STAGE_BYTES;      // float [M][MSTRIDE]
   static constexpr int OFF_MROW = OFF_MERGE + M * MSTRIDE * 4; // float [KGW][M]
   static constexpr int OFF_LROW = OFF_MROW + KGW * M * 4;      // float [M]
-  static constexpr int OFF_CNT = OFF_LROW + M * 4;             // uint32 [kStages] warps done per stage
-  static constexpr int OFF_BAR = (OFF_CNT + kStages * 4 + 7) & ~7;
-  static constexpr int OFF_META = OFF_BAR + kStages * 8;       // int cum[B+1], nlen[B]
+  static constexpr int OFF_BAR = (OFF_LROW + M * 4 + 7) & ~7;  // full[kStages], empty[kStages]
+  static constexpr int OFF_META = OFF_BAR + 2 * kStages * 8;   // int cum[B+1], nlen[B]
   static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
 };
 
@@ -121,8 +120,8 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
   float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
   float* mrow = reinterpret_cast<float*>(smem + C::OFF_MROW);
   float* lrow = reinterpret_cast<float*>(smem + C::OFF_LROW);
-  uint32_t* done = reinterpret_cast<uint32_t*>(smem + C::OFF_CNT);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + kStages;
   int* cum = reinterpret_cast<int*>(smem + C::OFF_META);
   int* nlen = cum + p.B + 1;
 
@@ -131,7 +130,7 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      done[s] = 0u;
+      mbar_init(&empty[s], C::W);
     }
     fence_mbar_init();
   }
@@ -146,9 +145,10 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
   const int t1 = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas));
   if (t0 >= t1) return;
 
-  // The ring holds tiles x .. x + kStages - 1.  Thread 0 fills it first; afterwards
-  // the last warp to finish a tile refills that stage with tile x + kStages, so no
-  // warp ever waits for the others between tiles.
+  // The ring holds tiles x .. x + kStages - 1.  Thread 0 fills it first; every warp
+  // arrives on a stage's empty barrier when done with its tile, and after finishing
+  // tile x thread 0 refills the stage of tile x - 1 (normally released by then)
+  // with tile x - 1 + kStages.  No warp waits for the others between tiles.
   auto issue = [&](int stage, int tile) {
     int ib, ig, ij;
     locate(tile, cum, p.B, p.Hkv, ib, ig, ij);
@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
   const int vt1 = row1 < p.M ? row1 / p.G : -1;
   const bool r0m0 = vt0 >= 0 && ((p.mask0 >> vt0) & 1u), r1m0 = vt1 >= 0 && ((p.mask0 >> vt1) & 1u);
   const bool r0m1 = vt0 >= 0 && ((p.mask1 >> vt0) & 1u), r1m1 = vt1 >= 0 && ((p.mask1 >> vt1) & 1u);
-  const bool any_mask = (p.mask0 | p.mask1) != 0;
   const float NEG = neg_inf();
 
   int b, g, j;
@@ -238,38 +237,22 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
         float s[2][4];
         qk16<D>(qf, kaddr, s, lane);
         const int key0 = j * TK + kg * 16;
-        if (any_mask) {  // logit sums over this warp's rows of each mask, then over lanes sharing a key
-          float v0[4], v1[4];
+        // logit sums over this warp's rows of each mask (column sums of S), written
+        // as this m-tile's share of the KV head's score of each key
+        const int skey = key0 + ((lane >> 4) & 1) * 8 + tig * 2 + ((lane >> 3) & 1);
+#pragma unroll
+        for (int ms = 0; ms < 2; ++ms) {
+          if ((ms ? p.mask1 : p.mask0) == 0u) continue;
+          const bool m0 = ms ? r0m1 : r0m0, m1 = ms ? r1m1 : r1m0;
+          float v[4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const float a = s[nt][c], bq = s[nt][2 + c];
-              v0[nt * 2 + c] = (r0m0 ? a : 0.f) + (r1m0 ? bq : 0.f);
-              v1[nt * 2 + c] = (r0m1 ? a : 0.f) + (r1m1 ? bq : 0.f);
-            }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-              v0[i] += __shfl_xor_sync(0xffffffffu, v0[i], off);
-              v1[i] += __shfl_xor_sync(0xffffffffu, v1[i], off);
-            }
-          }
-          if (gid == 0) {  // this m-tile's share of the KV head's score of each key
-            float* s0 = p.part_s + (((static_cast<size_t>(0) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len;
-            float* s1 = p.part_s + (((static_cast<size_t>(1) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int pos = key0 + nt * 8 + tig * 2 + c;
-                if (pos < n_b) {
-                  if (p.mask0) s0[pos] = v0[nt * 2 + c] * p.scale;
-                  if (p.mask1) s1[pos] = v1[nt * 2 + c] * p.scale;
-                }
-              }
-          }
+            for (int c = 0; c < 2; ++c) v[nt * 2 + c] = (m0 ? s[nt][c] : 0.f) + (m1 ? s[nt][2 + c] : 0.f);
+          const float sum = colsum16(v, lane);
+          if ((lane & 4) == 0 && skey < n_b)
+            p.part_s[(((static_cast<size_t>(ms) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len + skey] =
+                sum * p.scale;
         }
         // softmax in log2 units; keys past the prefix end are masked
 #pragma unroll
@@ -283,11 +266,11 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
         softmax_pv16<D>(st, s, vaddr, lane);
       }
       __syncwarp();
-      if (lane == 0) {  // the last warp done with this stage refills it
-        if (atom_add_acq_rel_smem(&done[stage], 1u) == C::W - 1) {
-          done[stage] = 0u;
-          if (x + kStages < t1) issue(stage, x + kStages);
-        }
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (threadIdx.x == 0 && x > t0 && x - 1 + kStages < t1) {
+        const int lp = x - 1 - t0;  // the previous tile's place in the ring
+        if (mbar_wait(&empty[lp % kStages], static_cast<uint32_t>((lp / kStages) & 1), p.status))
+          issue(lp % kStages, x - 1 + kStages);
       }
       if (++stage == kStages) {
         stage = 0;
@@ -357,7 +340,15 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
     const size_t pair = static_cast<size_t>(b) * p.Hkv + g;
     float* cm = cs;
     float* csum = cs + p.nctas * G;
-    // phase 1: one round of independent loads into shared memory
+    // phase 1: one round of independent loads - each warp's partial output rows into
+    // registers, the verify rows' q/k/v and every partial's max/sum into shared memory
+    constexpr int NB = 16;
+    PartialRows<D, NB> pre;
+    const int jw = warp < G ? warp : 0;  // the row this warp merges first
+    auto orow = [&](int si) {
+      return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + t * G + jw) * D;
+    };
+    pre.load(orow, 0, 1, nseg, lane);
     constexpr int CH = D / 8;  // 16-byte chunks per row
     const __nv_bfloat16* qbase = p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G) * D;
     for (int e = tid; e < G * CH; e += 128)
@@ -403,9 +394,13 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
       for (int q = 0; q < PER; ++q) acc[q] = 0.f;
       float l = 0.f;
       const int m = t * G + jh;
-      merge_partials<D>(cm + jh, csum + jh, G, nseg, M,
-                        [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + m) * D; },
-                        acc, l, lane);
+      auto orow_j = [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + m) * D; };
+      if (jh == warp) {  // first row of this warp: most partials are already in registers
+        pre.accumulate(cm + jh, csum + jh, G, 0, 1, nseg, M, acc, l);
+        merge_partials<D>(cm + jh, csum + jh, G, nseg, M, orow_j, acc, l, lane, NB, 1);
+      } else {
+        merge_partials<D>(cm + jh, csum + jh, G, nseg, M, orow_j, acc, l, lane);
+      }
       for (int u = 0; u <= t; ++u) {
         const float w = ex2(lg[jh][u] - M);
         l += w;

@@ -332,7 +332,7 @@ vg_status check_draft_args(const DraftArgs& a) {
 
 vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, void* ws, const WsLayout& w,
                     const DevInfo& di, int32_t* dev_status, cudaStream_t stream, bool pdl) {
-  if (draft_smem_bytes(s.D, s.Hkv, s.B) > di.smem_optin)
+  if (draft_smem_bytes(s.D, s.Hkv) > di.smem_optin)
     return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d needs more shared memory than a CTA has",
                 s.Hkv * s.D);
   DraftParams p = {};
@@ -357,7 +357,6 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.nctas = di.sms;
-  p.meta = at<int32_t>(ws, w.dmeta);
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);
   p.out = static_cast<__nv_bfloat16*>(a.out);

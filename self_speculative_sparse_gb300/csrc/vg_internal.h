@@ -12,8 +12,8 @@ namespace vg {
 
 // Keys per verify tile: the unit of TMA transfer and of the work split.
 constexpr int kVerifyTileKeys = 64;
-// Prefix positions per score-reduction block of the verify combine kernel.
-constexpr int kScoreChunk = 1024;
+// Prefix positions per score-reduction block of the verify combine kernel (one per thread).
+constexpr int kScoreChunk = 128;
 // Longest draft-token tail a sparse draft step attends besides the selection.
 constexpr int kDraftMaxTail = 64;
 // Largest sequence the top-k kernel holds in shared memory across a cluster of 8.
@@ -76,7 +76,6 @@ struct DraftParams {
   int B, Hq, Hkv, G, D;
   float scale, scale_log2;
   int nctas;
-  int32_t* meta;               // [B + 1] entry prefix sums
   float* part_o;               // [nctas + B][Hq][D]  unnormalised partial outputs
   float* part_ml;              // [nctas + B][Hq][2]
   __nv_bfloat16* out;          // [B][Hq][D]
@@ -90,6 +89,6 @@ size_t verify_smem_bytes(int D, int Mpad, int B);
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
 size_t topk_smem_bytes(int per_cta);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
-size_t draft_smem_bytes(int D, int Hkv, int B);
+size_t draft_smem_bytes(int D, int Hkv);
 
 }  // namespace vg

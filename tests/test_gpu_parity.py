@@ -145,3 +145,61 @@ def test_device_bounds_are_reported_not_faulted():
     torch.cuda.synchronize()
     assert st2.check_status() == vb.VG_ERR_DEVICE_BOUNDS
     assert torch.isfinite(st2.out_draft[0].float()).all()
+
+
+def test_topk_repeated_runs_are_identical_and_exact():
+    """Many launches of the multi-CTA selection on one input: a race would show."""
+    from self_speculative_sparse_gb300 import binding as vb
+    rng = np.random.default_rng(11)
+    lens = [32768, 32768, 20000]
+    B, L = len(lens), max(lens)
+    sc = (rng.standard_normal((B, L)) * 10).astype(np.float32)
+    sc[1, ::7] = 3.0                                                  # a block of exact ties
+    dev = torch.from_numpy(sc).cuda()
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = 2048
+    want = [oracle.select_topk(sc[b, :n].astype(np.float64), k) for b, n in enumerate(lens)]
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    for rep in range(50):
+        idx.fill_(123456)
+        vb.vg_topk_select(dev, L, lt, B, L, k, idx, cnt, dev_status=status)
+        torch.cuda.synchronize()
+        gi = idx.cpu().numpy()
+        for b in range(B):
+            assert np.array_equal(gi[b], want[b]), (rep, b)
+    assert int(status.item()) == 0
+
+
+def test_graph_replay_rotation_keeps_status_clean():
+    """The benchmark's flow: CUDA-graph replays of verify/select/draft over rotating
+    cache copies, with the public draft entry point and a device tail-length array."""
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = scaled(W["llama8b"], n=4000, k=512)
+    pool = w.layer_pool(0)
+    ncopy = 3
+    states = [LayerState(w, pool) for _ in range(ncopy)]
+    tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device="cuda") for s in range(w.gamma)]
+
+    def draft_phase(st):
+        for s in range(w.gamma):
+            st.draft_step(s, tl[s])
+
+    for st in states:
+        st.iteration(select_extra=False)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(ncopy):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            a, b = states[c], states[(c + 1) % ncopy]
+            a.verify()
+            a.select()
+            draft_phase(b)
+        graphs.append(g)
+    for i in range(60):
+        graphs[i % ncopy].replay()
+    torch.cuda.synchronize()
+    assert [st.check_status() for st in states] == [0] * ncopy
+    check_iteration(w, pool, states[0], w.rows(w.select_rows), None)
