@@ -195,6 +195,28 @@ vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_i
                        int32_t k, uint32_t row_mask0, uint32_t row_mask1, vg_iter_outputs* out,
                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/*
+ * vg_sparse_draft_attn without a workspace argument.  This entry point has no
+ * counterpart in the paper; it exists for callers that cannot hand the library
+ * device memory, for example a host that must not call cudaMalloc during decoding
+ * (the call can synchronise the device and stall other streams) or that has no
+ * workspace to offer.  Same computation, arguments and results as
+ * vg_sparse_draft_attn; the scratch space comes from an 8 MiB area inside the
+ * library that every GPU using the library keeps until the process exits.
+ *   - It allocates and frees nothing.
+ *   - Dimensions whose draft scratch exceeds 8 MiB are rejected with
+ *     VG_ERR_WORKSPACE (for 152 SMs: about H_q * (152 + B) * (d + 2) * 4 bytes).
+ *   - The first call on each device looks up the area's device address; make that
+ *     first call before any stream capture.
+ *   - All calls share the one area, which keeps the last call's contents (nothing
+ *     in it needs to start at zero).  Calls that may overlap on the GPU - on
+ *     different streams, or from different host threads - race on it; order them.
+ */
+vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* cache, const void* q,
+                                       const void* k_new, const void* v_new, const int32_t* idx,
+                                       const int32_t* count, int32_t k_stride, const int32_t* tail_start,
+                                       const int32_t* tail_len, void* out, int32_t* dev_status, void* stream);
+
 /* Bytes of workspace any call above needs for these dimensions on the current
  * device (0 on invalid dims or no device; see vg_last_error()). */
 size_t vg_workspace_size(const vg_dims* dims, int32_t k);

@@ -23,7 +23,7 @@ VG_ERR_DEVICE_TIMEOUT = -5
 VG_ERR_DEVICE_BOUNDS = -6
 
 ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_sparse_draft_attn", "vg_iteration",
-                "vg_workspace_size", "vg_last_error", "vg_version")
+                "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_last_error", "vg_version")
 
 
 class VgError(RuntimeError):
@@ -76,6 +76,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_sparse_draft_attn.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), vp, vp, vp, vp, vp,
                                        i32, vp, vp, vp, vp, sz, vp, vp]
     L.vg_sparse_draft_attn.restype = i32
+    L.vg_sparse_draft_attn_noalloc.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), vp, vp, vp,
+                                               vp, vp, i32, vp, vp, vp, vp, vp]
+    L.vg_sparse_draft_attn_noalloc.restype = i32
     L.vg_iteration.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), ctypes.POINTER(vg_iter_inputs),
                                i32, u32, u32, ctypes.POINTER(vg_iter_outputs), vp, sz, vp, vp]
     L.vg_iteration.restype = i32
@@ -156,3 +159,11 @@ def vg_iteration(dims, cache, inputs: vg_iter_inputs, k, row_mask0, row_mask1, o
     wsb = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
     _check(load().vg_iteration(ctypes.byref(dims), ctypes.byref(cache), ctypes.byref(inputs), k, row_mask0,
                                row_mask1, ctypes.byref(outputs), ptr(ws), wsb, ptr(dev_status), _stream(stream)))
+
+
+def vg_sparse_draft_attn_noalloc(dims, cache, q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, out,
+                                 dev_status=None, stream=None) -> None:
+    """vg_sparse_draft_attn with the library's built-in scratch area instead of a workspace."""
+    _check(load().vg_sparse_draft_attn_noalloc(ctypes.byref(dims), ctypes.byref(cache), ptr(q), ptr(k_new),
+                                               ptr(v_new), ptr(idx), ptr(count), k_stride, ptr(tail_start),
+                                               ptr(tail_len), ptr(out), ptr(dev_status), _stream(stream)))

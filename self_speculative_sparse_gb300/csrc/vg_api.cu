@@ -496,4 +496,65 @@ vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_i
   return VG_OK;
 }
 
+// ---------------------------------------------------------------- no-allocation draft step
+// Some callers cannot give this library device memory: a host that runs the
+// draft step from a context where it must not call cudaMalloc (the call can
+// synchronise the device and stall other streams), or one that has no workspace
+// to hand over.  vg_sparse_draft_attn_noalloc serves them from a fixed scratch
+// area that lives in the library itself.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB per device, held until the process exits
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of g_noalloc_scratch on the current device (the host-side
+// symbol is only a stand-in).  Looked up once per device, on that device.
+vg_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(VG_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return VG_OK;
+}
+
+}  // namespace
+
+vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* cache, const void* q,
+                                       const void* k_new, const void* v_new, const int32_t* idx,
+                                       const int32_t* count, int32_t k_stride, const int32_t* tail_start,
+                                       const int32_t* tail_len, void* out, int32_t* dev_status, void* stream) {
+  g_err.clear();
+  Shape s;
+  vg_status st = check_dims(dims, &s);
+  if (st != VG_OK) return st;
+  if ((st = check_cache(cache)) != VG_OK) return st;
+  if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
+  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
+  if ((st = check_draft_args(a)) != VG_OK) return st;
+  DevInfo di;
+  if ((st = device_info(&di)) != VG_OK) return st;
+  const WsLayout w = ws_layout(s, di.sms);
+  const size_t dsegs = static_cast<size_t>(di.sms) + s.B;
+  const size_t need = w.dpart_ml + dsegs * s.Hq * 2 * 4;  // end of the draft step's scratch
+  if (need > kNoAllocScratchBytes)
+    return fail(VG_ERR_WORKSPACE,
+                "no-allocation draft step needs %zu bytes of scratch for these dims; its built-in area holds %zu "
+                "(use vg_sparse_draft_attn with a workspace)",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != VG_OK) return st;
+  return run_draft(s, cache, a, scratch, w, di, dev_status, static_cast<cudaStream_t>(stream), true);
+}
+
 }  // extern "C"
