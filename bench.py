@@ -165,14 +165,24 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(kernel_file: str, workload: str):
+VERIFY_SOURCES = ("verify_attn.cu", "attn_frag.cuh", "vg_common.cuh", "vg_internal.h")
+
+
+def verify_source_sha() -> str:
+    """sha256 over the sources the verify kernel is compiled from."""
+    h = hashlib.sha256()
+    for f in VERIFY_SOURCES:
+        h.update(open(os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
     """Per-launch DRAM bytes of the verify kernel from the committed ncu summary, if it
-    was taken on the current source (the summary records the source's sha256)."""
-    src = os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", kernel_file)
+    was taken on the current sources (the summary records their sha256)."""
     prof = os.path.join(ROOT, "profiles", f"verify_attn_{workload}.md")
-    if not (os.path.exists(src) and os.path.exists(prof)):
+    if not os.path.exists(prof):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = verify_source_sha()
     vals = {}
     for line in open(prof):
         if ":" in line and line.strip().startswith("- "):
@@ -398,7 +408,7 @@ def run_ours(args, rank, local, world):
         "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine)", "bound": "hbm",
                      "achieved": verify_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": verify_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": profiled_traffic("verify_attn.cu", w.name),
+                     "traffic": profiled_traffic(w.name),
                      "algorithmic_bytes": nbytes["verify"]},
         "e2e": {"value": e2e_s / e2e_steps * 1e6 / world, "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
