@@ -1,4 +1,4 @@
-// Verification attention with fused logit aggregation.
+// Verification attention with fused logit aggregation, on 5th-generation tensor cores.
 //
 // Vegas §2 step 1 (verification phase): the gamma+1 verify rows attend, with full
 // attention, every prefix entry and the verify rows up to themselves; the same pass
@@ -9,17 +9,26 @@
 //
 // GB300 design.  The work is the flattened list of (sequence, KV head, 64-key tile)
 // items, split evenly over one persistent CTA per SM (ragged batches balance by
-// construction).  Thread 0 of each CTA streams K and V tiles with 2-D TMA
-// (128-byte swizzled boxes) into a 5-stage shared-memory ring guarded by
-// mbarriers; 8 or 12 warps hold the G*(gamma+1) query rows of the current KV head
-// as tensor-core fragments and run QK^T and PV on bf16 MMA with fp32
-// accumulators and an online softmax.  The logit sums are taken from the same
-// QK^T fragments, so the cache is read exactly once.  Each contiguous run of tiles
-// of one (sequence, KV head) leaves one unnormalised partial (max, sum, O); a
-// combine kernel, launched as a programmatic dependent of this one, merges the
-// partials with the verify rows' own causal keys, writes bf16 outputs, appends the
-// verify rows' K/V to the cache and sums the per-KV-head partial scores in a fixed
-// order (deterministic, no atomics).
+// construction).  Each CTA runs three roles:
+//   warp 4   streams K and V tiles by 2-D TMA (128-byte swizzle) into a ring of
+//            shared-memory stages;
+//   warp 5   issues tcgen05.mma from one thread: S = Q K^T into a double-buffered
+//            tensor-memory tile, then O += P V into a tensor-memory accumulator;
+//   warps 0-3 own the 128 tensor-memory lanes, one A-operand row each: the G*(gamma+1)
+//            query rows of the current KV head, then two rows per score mask that
+//            hold the mask's summed query split into a bf16 high and low part.
+// A row thread reads its row of S, runs the online softmax on it alone (max and sum
+// are thread-local; the running max is raised only when a tile exceeds it by more
+// than 2^8, after which the thread rescales its row of O in tensor memory), and
+// writes its row of P (bf16) to shared memory for the P V product.  A score-row
+// thread's S row is already the summed logit q_sum . k of each key of the tile
+// (high part plus low part), so the aggregation costs two rows of the same MMA and
+// no shuffles; the cache is read exactly once.  Each contiguous run of tiles of one
+// (sequence, KV head) leaves one unnormalised partial (max, sum, O); a combine
+// kernel, launched as a programmatic dependent of this one, merges the partials
+// with the verify rows' own causal keys, writes bf16 outputs, appends the verify
+// rows' K/V to the cache and sums the per-KV-head partial scores in a fixed order
+// (deterministic, no atomics).
 #include <cstdio>
 
 #include "attn_frag.cuh"
@@ -30,27 +39,32 @@ namespace vg {
 namespace {
 
 constexpr int TK = kVerifyTileKeys;
-constexpr int kStages = 5;
+// A row's running max is raised only when a tile's max exceeds it by more than this
+// (log2 units), so P stays below 2^8 and rescaling O is rare.
+constexpr float kRescaleSlack = 8.f;
 
-template <int D, int MT>
-struct VCfg {
-  static constexpr int KGW = (MT == 4) ? 2 : 4;  // key-group warps per 16-row m-tile
-  static constexpr int KPW = 4 / KGW;            // 16-key groups per warp per tile
-  static constexpr int W = MT * KGW;             // warps (a multiple of 4: one share per SM sub-partition)
-  static constexpr int THREADS = W * 32;
-  static constexpr int HALVES = D / 64;          // 64-column (128-byte) swizzled boxes
-  static constexpr int HALF_BYTES = TK * 128;
+template <int D>
+struct TCfg {
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int HALVES = D / 64;             // 64-column (128-byte) swizzled boxes
+  static constexpr int HALF_BYTES = TK * 128;       // one box of a K or V tile
   static constexpr int TILE_BYTES = TK * D * 2;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int M = MT * 16;
-  static constexpr int MSTRIDE = D + 8;                        // padded merge rows: 2-way at most
-  static constexpr int OFF_MERGE = kStages * STAGE_BYTES;      // float [M][MSTRIDE]
-  static constexpr int OFF_MROW = OFF_MERGE + M * MSTRIDE * 4; // float [KGW][M]
-  static constexpr int OFF_LROW = OFF_MROW + KGW * M * 4;      // float [M]
-  static constexpr int OFF_BAR = (OFF_LROW + M * 4 + 7) & ~7;  // full[kStages], empty[kStages]
-  static constexpr int OFF_META = OFF_BAR + 2 * kStages * 8;   // int cum[B+1], nlen[B]
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile, then V tile
+  static constexpr int QHALF = 128 * 128;           // A operand: 128 rows x 64 columns
+  static constexpr int P_BYTES = 128 * TK * 2;      // P: 128 rows x 64 keys (one box wide)
+  static constexpr int OFF_Q = kStages * STAGE_BYTES;
+  static constexpr int OFF_P = OFF_Q + HALVES * QHALF;  // two P buffers
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin
+  static constexpr int NBAR = 2 * kStages + 10;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_META = OFF_TMEM + 16;    // int cum[B+1], nlen[B]
+  static constexpr int THREADS = 192;               // warps 0-3 rows, 4 TMA, 5 MMA
+  static constexpr uint32_t TMEM_COLS = 256;        // O at columns [0, D), S buffers at 128 and 192
+  static constexpr uint32_t COL_S = 128;
   static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
 };
+
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
@@ -110,31 +124,74 @@ __device__ __forceinline__ void advance(int& b, int& g, int& j, const int* cum, 
   }
 }
 
-template <int D, int MT>
-__global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
+
+// A wait every lane of the warp takes together (so a lost wait cannot split the warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+template <int D>
+__global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
     verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  using C = VCfg<D, MT>;
+  using C = TCfg<D>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
-  float* mrow = reinterpret_cast<float*>(smem + C::OFF_MROW);
-  float* lrow = reinterpret_cast<float*>(smem + C::OFF_LROW);
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sP = smem + C::OFF_P;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + S;
+  uint64_t* s_full = full + 2 * S;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_full + 4;
+  uint64_t* p_free = s_full + 6;
+  uint64_t* q_ready = s_full + 8;
+  uint64_t* fin = s_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   int* cum = reinterpret_cast<int*>(smem + C::OFF_META);
   int* nlen = cum + p.B + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsc = 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));  // score rows
+  const int arows = p.M + nsc;                                   // A-operand rows in use
+
   if (warp == 0) seq_meta(p, cum, nlen);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::W);
+      mbar_init(&empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&p_free[s], 1);
+    }
+    mbar_init(q_ready, 4);
+    mbar_init(fin, 1);
     fence_mbar_init();
   }
+  if (warp == 5) tc_alloc(tmem_slot, C::TMEM_COLS);
+  // A-operand rows no segment writes stay zero: Q rows >= arows, P rows >= M
+  {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    const int qz = (128 - arows) * 8;
+    for (int e = threadIdx.x; e < C::HALVES * qz; e += C::THREADS) {
+      const int h = e / qz, r = arows + (e - h * qz) / 8, c = e & 7;
+      *reinterpret_cast<uint4*>(sQ + h * C::QHALF + r * 128 + c * 16) = z;
+    }
+    const int pz = (128 - p.M) * 8;
+    for (int e = threadIdx.x; e < 2 * pz; e += C::THREADS) {
+      const int buf = e / pz, r = p.M + (e - buf * pz) / 8, c = e & 7;
+      *reinterpret_cast<uint4*>(sP + buf * C::P_BYTES + r * 128 + c * 16) = z;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_slot;
   if (blockIdx.x == 0) {  // the combine kernel reads these after this grid completes
     for (int i = threadIdx.x; i < 2 * p.B + 1; i += blockDim.x) p.meta[i] = cum[i];
   }
@@ -142,149 +199,260 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
 
   const int T = p.Hkv * cum[p.B];
   const int t0 = static_cast<int>(split_begin(blockIdx.x, T, p.nctas));
-  const int t1 = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas));
-  if (t0 >= t1) return;
+  const int ntiles = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas)) - t0;
 
-  // The ring holds tiles x .. x + kStages - 1.  Thread 0 fills it first; every warp
-  // arrives on a stage's empty barrier when done with its tile, and after finishing
-  // tile x thread 0 refills the stage of tile x - 1 (normally released by then)
-  // with tile x - 1 + kStages.  No warp waits for the others between tiles.
-  auto issue = [&](int stage, int tile) {
-    int ib, ig, ij;
-    locate(tile, cum, p.B, p.Hkv, ib, ig, ij);
-    fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
-    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-    uint8_t* kdst = smem + stage * C::STAGE_BYTES;
-    uint8_t* vdst = kdst + C::TILE_BYTES;
-    const int y = static_cast<int>(p.seq_offset[ib] + static_cast<int64_t>(ij) * TK);
-#pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, ig * D + h * 64, y, &full[stage]);
-      tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, ig * D + h * 64, y, &full[stage]);
-    }
-  };
-  if (threadIdx.x == 0) {
+  if (ntiles > 0 && warp == 4 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    int b, g, j;
+    locate(t0, cum, p.B, p.Hkv, b, g, j);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    for (int st = 0; st < kStages && t0 + st < t1; ++st) issue(st, t0 + st);
-  }
-
-  constexpr int NT = C::THREADS;
-  const int mt = warp % MT, kgw = warp / MT;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int row0 = mt * 16 + gid, row1 = row0 + 8;
-  const int vt0 = row0 < p.M ? row0 / p.G : -1;  // verify row of each fragment row
-  const int vt1 = row1 < p.M ? row1 / p.G : -1;
-  const bool r0m0 = vt0 >= 0 && ((p.mask0 >> vt0) & 1u), r1m0 = vt1 >= 0 && ((p.mask0 >> vt1) & 1u);
-  const bool r0m1 = vt0 >= 0 && ((p.mask1 >> vt0) & 1u), r1m1 = vt1 >= 0 && ((p.mask1 >> vt1) & 1u);
-  const float NEG = neg_inf();
-
-  int b, g, j;
-  locate(t0, cum, p.B, p.Hkv, b, g, j);
-  int stage = 0;
-  uint32_t phase = 0;
-  bool lost = false;
-  int x = t0;
-  while (x < t1 && !lost) {
-    const int tiles_b = cum[b + 1] - cum[b];
-    const int seg_end = min(t1, x + (tiles_b - j));
-    const int n_b = nlen[b];
-
-    // query rows of this (sequence, KV head): row m -> (t = m / G, head g*G + m % G)
-    uint32_t qf[D / 16][4];
-    load_q_frags<D>(qf,
-                    row0 < p.M ? p.q + ((static_cast<size_t>(b) * p.R + vt0) * p.Hq + g * p.G + row0 % p.G) * D
-                               : nullptr,
-                    row1 < p.M ? p.q + ((static_cast<size_t>(b) * p.R + vt1) * p.Hq + g * p.G + row1 % p.G) * D
-                               : nullptr,
-                    tig);
-    RowState<D> st;
-    st.init();
-
-    for (; x < seg_end; ++x, ++j) {
-      if (!mbar_wait(&full[stage], phase, p.status)) {
-        lost = true;
-        break;
+    int issued = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % S;
+      if (i >= S && !mbar_wait(&empty[st], ((i / S) - 1) & 1, p.status)) break;
+      fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
+      mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+      uint8_t* kdst = smem + st * C::STAGE_BYTES;
+      uint8_t* vdst = kdst + C::TILE_BYTES;
+      const int y = static_cast<int>(p.seq_offset[b] + static_cast<int64_t>(j) * TK);
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, g * D + h * 64, y, &full[st]);
+        tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, g * D + h * 64, y, &full[st]);
       }
-      const int valid = n_b - j * TK;  // keys of this tile inside the prefix
-      if (valid < TK) {  // (at most once per run of tiles, the only point where warps meet)
-        // The rows past the prefix end hold whatever the cache has there; their
-        // probabilities are zero, and zeroed values keep 0 * V exact even if the
-        // slots hold non-finite garbage.
-        uint4* vrows = reinterpret_cast<uint4*>(smem + stage * C::STAGE_BYTES + C::TILE_BYTES);
-        const int per_half = TK * 8;  // 16-byte chunks in one 128-byte-wide box
-        for (int e = threadIdx.x; e < C::HALVES * per_half; e += NT) {
-          const int h = e / per_half, r = (e - h * per_half) >> 3;
-          if (r >= valid) vrows[e] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // before the next TMA write into this stage
-        named_bar(2, NT);
-      }
-      const uint32_t kb = smem_u32(smem + stage * C::STAGE_BYTES);
-      const uint32_t vb = kb + C::TILE_BYTES;
-#pragma unroll
-      for (int kp = 0; kp < C::KPW; ++kp) {
-        const int kg = kgw * C::KPW + kp;
-        // 128-byte swizzle of the TMA boxes: chunk c of row r sits at chunk c ^ (r & 7)
-        auto kaddr = [&](int r, int c16) {
-          const int rr = kg * 16 + r;
-          return kb + (c16 >> 3) * C::HALF_BYTES + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4);
-        };
-        auto vaddr = [&](int r, int c16) {
-          const int rr = kg * 16 + r;
-          return vb + (c16 >> 3) * C::HALF_BYTES + rr * 128 + (((c16 & 7) ^ (rr & 7)) << 4);
-        };
-        float s[2][4];
-        qk16<D>(qf, kaddr, s, lane);
-        const int key0 = j * TK + kg * 16;
-        // logit sums over this warp's rows of each mask (column sums of S), written
-        // as this m-tile's share of the KV head's score of each key
-        const int skey = key0 + ((lane >> 4) & 1) * 8 + tig * 2 + ((lane >> 3) & 1);
-#pragma unroll
-        for (int ms = 0; ms < 2; ++ms) {
-          if ((ms ? p.mask1 : p.mask0) == 0u) continue;
-          const bool m0 = ms ? r0m1 : r0m0, m1 = ms ? r1m1 : r1m0;
-          float v[4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) v[nt * 2 + c] = (m0 ? s[nt][c] : 0.f) + (m1 ? s[nt][2 + c] : 0.f);
-          const float sum = colsum16(v, lane);
-          if ((lane & 4) == 0 && skey < n_b)
-            p.part_s[(((static_cast<size_t>(ms) * p.B + b) * p.Hkv + g) * MT + mt) * p.max_len + skey] =
-                sum * p.scale;
-        }
-        // softmax in log2 units; keys past the prefix end are masked
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const bool ok = key0 + nt * 8 + tig * 2 + c < n_b;
-            s[nt][c] = ok ? s[nt][c] * p.scale_log2 : NEG;
-            s[nt][2 + c] = ok ? s[nt][2 + c] * p.scale_log2 : NEG;
-          }
-        softmax_pv16<D>(st, s, vaddr, lane);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (threadIdx.x == 0 && x > t0 && x - 1 + kStages < t1) {
-        const int lp = x - 1 - t0;  // the previous tile's place in the ring
-        if (mbar_wait(&empty[lp % kStages], static_cast<uint32_t>((lp / kStages) & 1), p.status))
-          issue(lp % kStages, x - 1 + kStages);
-      }
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1u;
-      }
+      ++issued;
+      advance(b, g, j, cum, p.B, p.Hkv);
     }
+    // no copy may still be in flight when the CTA exits (normally all were consumed)
+    for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
+  } else if (ntiles > 0 && warp == 5 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = tc_idesc_bf16(128, TK, 0, 0);
+    constexpr uint32_t idO = tc_idesc_bf16(128, D, 0, 1);
+    const uint32_t base = smem_u32(smem), qaddr = smem_u32(sQ), paddr = smem_u32(sP);
+    // O += P V for tile x (first: the first tile of its run, which overwrites O)
+    auto pv = [&](int x, bool first) -> bool {
+      if (!mbar_wait(&p_full[x & 1], (x >> 1) & 1, p.status)) return false;
+      tc_fence_after();
+      const int st = x % S;
+      const uint32_t vaddr = base + st * C::STAGE_BYTES + C::TILE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < TK / 16; ++kk)
+        tc_mma(tm, tc_desc_sw128(paddr + (x & 1) * C::P_BYTES + kk * 32, 16, 1024),
+               tc_desc_sw128(vaddr + kk * 2048, C::HALF_BYTES, 1024), idO, (kk > 0 || !first) ? 1u : 0u);
+      tc_commit(&empty[st]);
+      tc_commit(&p_free[x & 1]);
+      return true;
+    };
+    int b, g, j;
+    locate(t0, cum, p.B, p.Hkv, b, g, j);
+    int seg = 0;
+    bool prev_first = false, ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const bool first = (i == 0) || (j == 0);
+      // at a run boundary the row warps read O only after the previous run's last P V
+      if (i > 0 && first && !pv(i - 1, prev_first)) { ok = false; break; }
+      if (first) {
+        if (!mbar_wait(q_ready, seg & 1, p.status)) { ok = false; break; }
+        ++seg;
+      }
+      const int st = i % S;
+      if (!mbar_wait(&full[st], (i / S) & 1, p.status)) { ok = false; break; }
+      if (i >= 2 && !mbar_wait(&s_free[i & 1], ((i - 2) >> 1) & 1, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t kaddr = base + st * C::STAGE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma(tm + C::COL_S + (i & 1) * TK,
+               tc_desc_sw128(qaddr + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024),
+               tc_desc_sw128(kaddr + (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32, 16, 1024), idS,
+               kk > 0 ? 1u : 0u);
+      tc_commit(&s_full[i & 1]);
+      // steady state: the previous tile's P V goes after this tile's Q K^T, so the
+      // row warps find S ready as soon as they finish P
+      if (i > 0 && !first && !pv(i - 1, prev_first)) { ok = false; break; }
+      prev_first = first;
+      advance(b, g, j, cum, p.B, p.Hkv);
+    }
+    if (ok) pv(ntiles - 1, prev_first);
+    tc_commit(fin);  // every MMA of this thread complete before the CTA tears down
+    mbar_wait(fin, 0, p.status);
+  } else if (ntiles > 0 && warp < 4) {
+    // ---------------------------------------------------------------- row warps
+    const int tid = threadIdx.x;  // = tensor-memory lane = A-operand row
+    const uint32_t tl = tm + (static_cast<uint32_t>(32 * warp) << 16);
+    const bool wact = 32 * warp < arows;  // warp-uniform: lanes hold rows in use
+    const bool is_row = tid < p.M;
+    const int sci = tid - p.M;
+    const bool is_sc = sci >= 0 && sci < nsc;
+    const int sc_ms = (sci >> 1) == 0 && p.mask0 ? 0 : 1;  // score rows: mask0 first if in use
+    const int sc_part = sci & 1;
+    const float c2 = p.scale_log2;
+    const float NEG = neg_inf();
+    int b, g, j;
+    locate(t0, cum, p.B, p.Hkv, b, g, j);
+    bool ok = true;
+    int i = 0;
+    while (i < ntiles && ok) {
+      const int n_b = nlen[b];
+      const int seg_first = i;
+      const int seg_end = min(ntiles, i + (cum[b + 1] - cum[b] - j));
+      // query rows of this (sequence, KV head): row r -> (t = r / G, head g*G + r % G)
+      for (int e = tid; e < p.M * (D / 8); e += 128) {
+        const int r = e / (D / 8), c = e - r * (D / 8);
+        const int t = r / p.G, hh = r - t * p.G;
+        const uint4 v =
+            *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * p.G + hh) * D + c * 8);
+        *reinterpret_cast<uint4*>(sQ + (c >> 3) * C::QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+      }
+      named_bar(1, 128);
+      // score rows: column d of each mask's summed query, split into bf16 high + low
+      if (nsc > 0 && tid < D) {
+        const int cc = tid & 63;
+        int a = 0;
+        for (int ms = 0; ms < 2; ++ms) {
+          const uint32_t mk = ms ? p.mask1 : p.mask0;
+          if (mk == 0u) continue;
+          float acc = 0.f;
+          for (int r = 0; r < p.M; ++r) {
+            if (((mk >> (r / p.G)) & 1u) == 0u) continue;
+            acc += bf2f(*reinterpret_cast<const __nv_bfloat16*>(sQ + (tid >> 6) * C::QHALF + r * 128 +
+                                                                 (((cc >> 3) ^ (r & 7)) << 4) + (cc & 7) * 2));
+          }
+          const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(acc - bf2f(hi));
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const int r = p.M + 2 * a + part;
+            *reinterpret_cast<__nv_bfloat16*>(sQ + (tid >> 6) * C::QHALF + r * 128 + (((cc >> 3) ^ (r & 7)) << 4) +
+                                              (cc & 7) * 2) = part ? lo : hi;
+          }
+          ++a;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
 
-    // segment partial: merge the key-group warps of each m-tile, then store
-    merge_warps<D, C::KGW>(st, C::M, C::MSTRIDE, row0, kgw, merge, mrow, lrow, tig, 1, NT);
-    const size_t id = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g;
-    store_partial<D, C::KGW>(merge, C::MSTRIDE, mrow, lrow, C::M, p.part_o + id * C::M * D,
-                             p.part_ml + id * C::M * 2, threadIdx.x, NT);
-    named_bar(1, NT);
-    if (x < t1) {  // next (sequence, KV head)
+      float m = NEG, l = 0.f;
+      for (; i < seg_end; ++i, ++j) {
+        const int valid = min(TK, n_b - j * TK);  // keys of this tile inside the prefix (>= 1)
+        if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, p.status)) { ok = false; break; }
+        tc_fence_after();
+        float s[TK];
+        if (wact) tc_ld64_sync(tl + C::COL_S + (i & 1) * TK, s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[i & 1]);
+        if (valid < TK) {
+          // rows past the prefix end hold whatever the cache has there; their P is
+          // zero, and zeroed V rows keep 0 * V exact even if the slots are not finite
+          if (!warp_wait(&full[i % S], (i / S) & 1, p.status)) { ok = false; break; }
+          uint8_t* vt = smem + (i % S) * C::STAGE_BYTES + C::TILE_BYTES;
+          for (int e = tid; e < C::HALVES * TK * 8; e += 128) {
+            const int h = e / (TK * 8), r = (e >> 3) & (TK - 1);
+            if (r >= valid)
+              *reinterpret_cast<uint4*>(vt + h * C::HALF_BYTES + r * 128 + (e & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        if (wact) {
+          float mx = NEG;
+          if (valid == TK) {
+#pragma unroll
+            for (int c = 0; c < TK; ++c) mx = fmaxf(mx, s[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < TK; ++c) mx = fmaxf(mx, c < valid ? s[c] : NEG);
+          }
+          mx *= c2;
+          const bool first = (i == seg_first);
+          const float mn = (is_row && (first || mx > m + kRescaleSlack)) ? fmaxf(m, mx) : m;
+          const bool resc = is_row && !first && mn != m;
+          if (__any_sync(0xffffffffu, resc)) {
+            // rare: the running max rises; rescale l and this row of O once P V of
+            // the previous tile has landed in tensor memory
+            const float alpha = resc ? ex2(m - mn) : 1.f;
+            l *= alpha;
+            if (!warp_wait(&p_free[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              float o[32];
+              tc_ld32_sync(tl + c0, o);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) o[q] *= alpha;
+              tc_st32(tl + c0, o);
+            }
+            tc_wait_st();
+          }
+          m = mn;
+          // P of this tile goes to the buffer P V of tile i - 2 read
+          if (i >= 2 && !warp_wait(&p_free[i & 1], ((i - 2) >> 1) & 1, p.status)) { ok = false; break; }
+          if (is_row) {
+            uint32_t pk[TK / 2];
+            float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < TK; c += 2) {
+              float p0 = ex2(fmaf(s[c], c2, -m)), p1 = ex2(fmaf(s[c + 1], c2, -m));
+              if (valid < TK) {
+                p0 = c < valid ? p0 : 0.f;
+                p1 = c + 1 < valid ? p1 : 0.f;
+              }
+              ls += p0 + p1;
+              pk[c / 2] = pack_bf16(p0, p1);
+            }
+            l += ls;
+            uint8_t* prow = sP + (i & 1) * C::P_BYTES + tid * 128;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+              *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
+                  make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          } else if (is_sc) {
+            float* dst = p.part_s +
+                         (((static_cast<size_t>(sc_ms) * p.B + b) * p.Hkv + g) * 2 + sc_part) * p.s_stride + j * TK;
+            if (valid == TK) {
+#pragma unroll
+              for (int c = 0; c < TK; c += 4)
+                *reinterpret_cast<float4*>(dst + c) =
+                    make_float4(s[c] * p.scale, s[c + 1] * p.scale, s[c + 2] * p.scale, s[c + 3] * p.scale);
+            } else {
+#pragma unroll
+              for (int c = 0; c < TK; ++c)
+                if (c < valid) dst[c] = s[c] * p.scale;
+            }
+          }
+        }
+        fence_proxy_async_smem();  // P (and zeroed V rows) before the async proxy reads them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[i & 1]);
+      }
+      if (!ok) break;
+      // run partial: (O, max, sum) of each query row once P V of its last tile landed
+      const int last = i - 1;
+      if (!warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status)) break;
+      tc_fence_after();
+      if (32 * warp < p.M) {
+        const size_t prow = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g) * p.Mpad + tid;
+        float* orow = p.part_o + prow * D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tc_ld32_sync(tl + c0, o);
+          if (is_row) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<float4*>(orow + c0 + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+          }
+        }
+        if (is_row) {
+          p.part_ml[prow * 2 + 0] = m;
+          p.part_ml[prow * 2 + 1] = l;
+        }
+      }
+      tc_fence_before();
+      // next (sequence, KV head)
       j = 0;
       if (++g == p.Hkv) {
         g = 0;
@@ -292,6 +460,13 @@ __global__ void __launch_bounds__(VCfg<D, MT>::THREADS, 1)
         while (b < p.B && cum[b + 1] == cum[b]) ++b;
       }
     }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tc_dealloc(tm, C::TMEM_COLS);
   }
 }
 
@@ -431,33 +606,33 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
   for (int ms = 0; ms < 2; ++ms) {
     float* dst = ms ? p.scores1 : p.scores0;
     if ((ms ? p.mask1 : p.mask0) == 0u || dst == nullptr) continue;
-    const int parts = p.Hkv * (p.Mpad / 16);  // (KV head, m-tile) shares, in a fixed order
-    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.max_len;
+    const int parts = p.Hkv * 2;  // (KV head, high / low part) shares, in a fixed order
+    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.s_stride;
     for (int pos = lo + tid; pos < hi; pos += 128) {
       float v = 0.f;
 #pragma unroll 8
-      for (int q = 0; q < parts; ++q) v += src[static_cast<size_t>(q) * p.max_len + pos];
+      for (int q = 0; q < parts; ++q) v += src[static_cast<size_t>(q) * p.s_stride + pos];
       dst[static_cast<size_t>(b) * p.score_stride + pos] = v;
     }
   }
 }
 
-template <int D, int MT>
+template <int D>
 cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             cudaStream_t stream) {
-  using C = VCfg<D, MT>;
+  using C = TCfg<D>;
   const size_t smem = C::smem(p.B);
-  cudaError_t e = ensure_smem<verify_kernel<D, MT>>(smem);
+  cudaError_t e = ensure_smem<verify_kernel<D>>(smem);
   if (e != cudaSuccess) return e;
-  verify_kernel<D, MT><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
+  verify_kernel<D><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, verify_kernel<D, MT>) == cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, verify_kernel<D>) == cudaSuccess) {
       fprintf(stderr,
-              "verify_kernel<%d,%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
+              "verify_kernel<%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
               "requestedSmem=%zu localBytes=%zu)\n",
-              D, MT, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, C::THREADS, fa.sharedSizeBytes,
+              D, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, C::THREADS, fa.sharedSizeBytes,
               fa.maxDynamicSharedSizeBytes, smem, fa.localSizeBytes);
     }
     return e;
@@ -479,24 +654,16 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
 
 }  // namespace
 
-size_t verify_smem_bytes(int D, int Mpad, int B) {
-  const int MT = Mpad / 16;
-#define VG_SMEM_CASE(DD, MM) \
-  if (D == DD && MT == MM) return VCfg<DD, MM>::smem(B);
-  VG_SMEM_CASE(64, 1) VG_SMEM_CASE(64, 2) VG_SMEM_CASE(64, 3) VG_SMEM_CASE(64, 4)
-  VG_SMEM_CASE(128, 1) VG_SMEM_CASE(128, 2) VG_SMEM_CASE(128, 3) VG_SMEM_CASE(128, 4)
-#undef VG_SMEM_CASE
+size_t verify_smem_bytes(int D, int B) {
+  if (D == 64) return TCfg<64>::smem(B);
+  if (D == 128) return TCfg<128>::smem(B);
   return 0;
 }
 
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream) {
-  const int MT = p.Mpad / 16;
-#define VG_LAUNCH_CASE(DD, MM) \
-  if (p.D == DD && MT == MM) return launch_verify_t<DD, MM>(p, tmK, tmV, stream);
-  VG_LAUNCH_CASE(64, 1) VG_LAUNCH_CASE(64, 2) VG_LAUNCH_CASE(64, 3) VG_LAUNCH_CASE(64, 4)
-  VG_LAUNCH_CASE(128, 1) VG_LAUNCH_CASE(128, 2) VG_LAUNCH_CASE(128, 3) VG_LAUNCH_CASE(128, 4)
-#undef VG_LAUNCH_CASE
+  if (p.D == 64) return launch_verify_t<64>(p, tmK, tmV, stream);
+  if (p.D == 128) return launch_verify_t<128>(p, tmK, tmV, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -159,6 +159,9 @@ struct WsLayout {
   size_t total = 0;
 };
 
+// Row stride of the per-KV-head partial scores: 16-byte-aligned rows for vector stores.
+inline int score_stride(const Shape& s) { return (s.max_len + 63) & ~63; }
+
 WsLayout ws_layout(const Shape& s, int sms) {
   WsLayout w;
   const size_t segs = static_cast<size_t>(sms) + static_cast<size_t>(s.B) * s.Hkv;
@@ -170,7 +173,7 @@ WsLayout ws_layout(const Shape& s, int sms) {
   w.part_ml = off;
   off = up256(off + segs * s.Mpad * 2 * 4);
   w.part_s = off;
-  off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * (s.Mpad / 16) * static_cast<size_t>(s.max_len) * 4);
+  off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * 2 * static_cast<size_t>(score_stride(s)) * 4);
   const size_t verify_total = off;
   const size_t dsegs = static_cast<size_t>(sms) + s.B;
   off = 0;  // the draft step's scratch reuses the same bytes (calls are stream-ordered)
@@ -226,8 +229,8 @@ vg_status check_verify_args(const Shape& s, const VerifyArgs& a) {
 
 vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, void* ws, const WsLayout& w,
                      const DevInfo& di, int32_t* dev_status, cudaStream_t stream) {
-  if (verify_smem_bytes(s.D, s.Mpad, s.B) > di.smem_optin)
-    return fail(VG_ERR_UNSUPPORTED_SHAPE, "verify needs %zu bytes of shared memory", verify_smem_bytes(s.D, s.Mpad, s.B));
+  if (verify_smem_bytes(s.D, s.B) > di.smem_optin)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "verify needs %zu bytes of shared memory", verify_smem_bytes(s.D, s.B));
   CUtensorMap tmK, tmV;
   vg_status st = encode_cache_map(&tmK, c->K, c->capacity_slots, s.Hkv, s.D);
   if (st != VG_OK) return st;
@@ -260,6 +263,7 @@ vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, 
   p.part_o = at<float>(ws, w.part_o);
   p.part_ml = at<float>(ws, w.part_ml);
   p.part_s = at<float>(ws, w.part_s);
+  p.s_stride = score_stride(s);
   p.scores0 = a.scores0;
   p.scores1 = a.scores1;
   p.score_stride = a.score_stride;

@@ -39,7 +39,8 @@ struct VerifyParams {
   int32_t* meta;     // [B + 1] tiles-per-head prefix sums, then [B] checked lengths
   float* part_o;     // [nctas + B*Hkv][Mpad][D]  unnormalised partial outputs
   float* part_ml;    // [nctas + B*Hkv][Mpad][2]  (running max in log2 units, sum)
-  float* part_s;     // [2][B][Hkv][Mpad/16][max_len]  per-(KV head, m-tile) partial scores
+  float* part_s;     // [2][B][Hkv][2][s_stride]  per-(KV head, high / low part) partial scores
+  int s_stride;      // max_len rounded up to a multiple of 64
   // outputs
   float* scores0;    // [B][score_stride] or null
   float* scores1;
@@ -85,7 +86,7 @@ struct DraftParams {
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream);
-size_t verify_smem_bytes(int D, int Mpad, int B);
+size_t verify_smem_bytes(int D, int B);
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
 size_t topk_smem_bytes(int per_cta);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
