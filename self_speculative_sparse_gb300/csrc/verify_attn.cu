@@ -10,17 +10,20 @@
 // GB300 design.  The work is the flattened list of (sequence, KV head, 64-key tile)
 // items, split evenly over one persistent CTA per SM (ragged batches balance by
 // construction).  Each CTA runs three roles:
-//   warp 4   streams K and V tiles by 2-D TMA (128-byte swizzle) into a ring of
+//   warp 8   streams K and V tiles by 2-D TMA (128-byte swizzle) into a ring of
 //            shared-memory stages;
-//   warp 5   issues tcgen05.mma from one thread: S = Q K^T into a double-buffered
+//   warp 9   issues tcgen05.mma from one thread: S = Q K^T into a double-buffered
 //            tensor-memory tile, then O += P V into a tensor-memory accumulator;
-//   warps 0-3 own the 128 tensor-memory lanes, one A-operand row each: the G*(gamma+1)
-//            query rows of the current KV head, then two rows per score mask that
-//            hold the mask's summed query split into a bf16 high and low part.
-// A row thread reads its row of S, runs the online softmax on it alone (max and sum
-// are thread-local; the running max is raised only when a tile exceeds it by more
-// than 2^8, after which the thread rescales its row of O in tensor memory), and
-// writes its row of P (bf16) to shared memory for the P V product.  A score-row
+//   warps 0-7 own the 128 tensor-memory lanes, one A-operand row per lane: the
+//            G*(gamma+1) query rows of the current KV head, then two rows per score
+//            mask that hold the mask's summed query split into a bf16 high and low
+//            part.  Warps w and w + 4 share lane quadrant w and take the low and high
+//            32 keys of each tile.
+// A row thread reads its half row of S and runs the online softmax on it (max and
+// sum are per thread; the two halves of a row agree on the tile max through shared
+// memory; the running max is raised only when a tile exceeds it by more than 2^8,
+// after which the row's O is rescaled in tensor memory), and writes its half row of
+// P (bf16) to shared memory for the P V product.  A score-row
 // thread's S row is already the summed logit q_sum . k of each key of the tile
 // (high part plus low part), so the aggregation costs two rows of the same MMA and
 // no shuffles; the cache is read exactly once.  Each contiguous run of tiles of one
@@ -58,8 +61,10 @@ struct TCfg {
   // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin
   static constexpr int NBAR = 2 * kStages + 10;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-  static constexpr int OFF_META = OFF_TMEM + 16;    // int cum[B+1], nlen[B]
-  static constexpr int THREADS = 192;               // warps 0-3 rows, 4 TMA, 5 MMA
+  static constexpr int OFF_X = OFF_TMEM + 16;       // float xm[2][2][128] tile maxima, xl[128] sums
+  static constexpr int OFF_META = OFF_X + 5 * 128 * 4;  // int cum[B+1], nlen[B]
+  static constexpr int RWARPS = 8;                  // row warps: two per tensor-memory lane quadrant
+  static constexpr int THREADS = (RWARPS + 2) * 32; // + TMA producer warp + MMA warp
   static constexpr uint32_t TMEM_COLS = 256;        // O at columns [0, D), S buffers at 128 and 192
   static constexpr uint32_t COL_S = 128;
   static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
@@ -164,15 +169,15 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);
-      mbar_init(&p_full[s], 4);
+      mbar_init(&s_free[s], C::RWARPS);
+      mbar_init(&p_full[s], C::RWARPS);
       mbar_init(&p_free[s], 1);
     }
-    mbar_init(q_ready, 4);
+    mbar_init(q_ready, C::RWARPS);
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  if (warp == 5) tc_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == C::RWARPS + 1) tc_alloc(tmem_slot, C::TMEM_COLS);
   // A-operand rows no segment writes stay zero: Q rows >= arows, P rows >= M
   {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -201,7 +206,7 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
   const int t0 = static_cast<int>(split_begin(blockIdx.x, T, p.nctas));
   const int ntiles = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas)) - t0;
 
-  if (ntiles > 0 && warp == 4 && lane == 0) {
+  if (ntiles > 0 && warp == C::RWARPS && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
     }
     // no copy may still be in flight when the CTA exits (normally all were consumed)
     for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
-  } else if (ntiles > 0 && warp == 5 && lane == 0) {
+  } else if (ntiles > 0 && warp == C::RWARPS + 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idS = tc_idesc_bf16(128, TK, 0, 0);
     constexpr uint32_t idO = tc_idesc_bf16(128, D, 0, 1);
@@ -278,18 +283,24 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
     if (ok) pv(ntiles - 1, prev_first);
     tc_commit(fin);  // every MMA of this thread complete before the CTA tears down
     mbar_wait(fin, 0, p.status);
-  } else if (ntiles > 0 && warp < 4) {
+  } else if (ntiles > 0 && warp < C::RWARPS) {
     // ---------------------------------------------------------------- row warps
-    const int tid = threadIdx.x;  // = tensor-memory lane = A-operand row
-    const uint32_t tl = tm + (static_cast<uint32_t>(32 * warp) << 16);
-    const bool wact = 32 * warp < arows;  // warp-uniform: lanes hold rows in use
-    const bool is_row = tid < p.M;
-    const int sci = tid - p.M;
+    constexpr int NR = C::RWARPS * 32;
+    constexpr int HK = TK / 2;            // keys of a tile per half
+    const int rtid = threadIdx.x;         // 0 .. NR-1, for cooperative loops
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;     // = tensor-memory lane = A-operand row
+    const uint32_t tl = tm + (static_cast<uint32_t>(32 * quad) << 16);
+    const bool wact = 32 * quad < arows;  // warp-uniform: lanes hold rows in use
+    const bool is_row = row < p.M;
+    const int sci = row - p.M;
     const bool is_sc = sci >= 0 && sci < nsc;
     const int sc_ms = (sci >> 1) == 0 && p.mask0 ? 0 : 1;  // score rows: mask0 first if in use
     const int sc_part = sci & 1;
     const float c2 = p.scale_log2;
     const float NEG = neg_inf();
+    float* xm = reinterpret_cast<float*>(smem + C::OFF_X);  // [tile parity][half][row]
+    float* xl = xm + 4 * 128;                               // [row]
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
     bool ok = true;
@@ -299,17 +310,17 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
       const int seg_first = i;
       const int seg_end = min(ntiles, i + (cum[b + 1] - cum[b] - j));
       // query rows of this (sequence, KV head): row r -> (t = r / G, head g*G + r % G)
-      for (int e = tid; e < p.M * (D / 8); e += 128) {
+      for (int e = rtid; e < p.M * (D / 8); e += NR) {
         const int r = e / (D / 8), c = e - r * (D / 8);
         const int t = r / p.G, hh = r - t * p.G;
         const uint4 v =
             *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * p.G + hh) * D + c * 8);
         *reinterpret_cast<uint4*>(sQ + (c >> 3) * C::QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
       }
-      named_bar(1, 128);
+      named_bar(1, NR);
       // score rows: column d of each mask's summed query, split into bf16 high + low
-      if (nsc > 0 && tid < D) {
-        const int cc = tid & 63;
+      if (nsc > 0 && rtid < D) {
+        const int cc = rtid & 63;
         int a = 0;
         for (int ms = 0; ms < 2; ++ms) {
           const uint32_t mk = ms ? p.mask1 : p.mask0;
@@ -317,7 +328,7 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
           float acc = 0.f;
           for (int r = 0; r < p.M; ++r) {
             if (((mk >> (r / p.G)) & 1u) == 0u) continue;
-            acc += bf2f(*reinterpret_cast<const __nv_bfloat16*>(sQ + (tid >> 6) * C::QHALF + r * 128 +
+            acc += bf2f(*reinterpret_cast<const __nv_bfloat16*>(sQ + (rtid >> 6) * C::QHALF + r * 128 +
                                                                  (((cc >> 3) ^ (r & 7)) << 4) + (cc & 7) * 2));
           }
           const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
             const int r = p.M + 2 * a + part;
-            *reinterpret_cast<__nv_bfloat16*>(sQ + (tid >> 6) * C::QHALF + r * 128 + (((cc >> 3) ^ (r & 7)) << 4) +
+            *reinterpret_cast<__nv_bfloat16*>(sQ + (rtid >> 6) * C::QHALF + r * 128 + (((cc >> 3) ^ (r & 7)) << 4) +
                                               (cc & 7) * 2) = part ? lo : hi;
           }
           ++a;
@@ -337,65 +348,72 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
 
       float m = NEG, l = 0.f;
       for (; i < seg_end; ++i, ++j) {
-        const int valid = min(TK, n_b - j * TK);  // keys of this tile inside the prefix (>= 1)
+        const int valid = min(TK, n_b - j * TK) - half * HK;  // keys of this half inside the prefix
         if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
-        float s[TK];
-        if (wact) tc_ld64_sync(tl + C::COL_S + (i & 1) * TK, s);
+        float s[HK];
+        if (wact) tc_ld32_sync(tl + C::COL_S + (i & 1) * TK + half * HK, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[i & 1]);
-        if (valid < TK) {
+        const int vt_keys = min(TK, n_b - j * TK);
+        if (vt_keys < TK) {
           // rows past the prefix end hold whatever the cache has there; their P is
           // zero, and zeroed V rows keep 0 * V exact even if the slots are not finite
           if (!warp_wait(&full[i % S], (i / S) & 1, p.status)) { ok = false; break; }
           uint8_t* vt = smem + (i % S) * C::STAGE_BYTES + C::TILE_BYTES;
-          for (int e = tid; e < C::HALVES * TK * 8; e += 128) {
+          for (int e = rtid; e < C::HALVES * TK * 8; e += NR) {
             const int h = e / (TK * 8), r = (e >> 3) & (TK - 1);
-            if (r >= valid)
+            if (r >= vt_keys)
               *reinterpret_cast<uint4*>(vt + h * C::HALF_BYTES + r * 128 + (e & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         if (wact) {
           float mx = NEG;
-          if (valid == TK) {
+          if (valid >= HK) {
 #pragma unroll
-            for (int c = 0; c < TK; ++c) mx = fmaxf(mx, s[c]);
+            for (int c = 0; c < HK; ++c) mx = fmaxf(mx, s[c]);
           } else {
 #pragma unroll
-            for (int c = 0; c < TK; ++c) mx = fmaxf(mx, c < valid ? s[c] : NEG);
+            for (int c = 0; c < HK; ++c) mx = fmaxf(mx, c < valid ? s[c] : NEG);
           }
           mx *= c2;
+          // both halves of the row take the max of the whole tile
+          xm[((i & 1) * 2 + half) * 128 + row] = mx;
+          named_bar(2 + quad, 64);
+          mx = fmaxf(mx, xm[((i & 1) * 2 + (half ^ 1)) * 128 + row]);
           const bool first = (i == seg_first);
           const float mn = (is_row && (first || mx > m + kRescaleSlack)) ? fmaxf(m, mx) : m;
           const bool resc = is_row && !first && mn != m;
           if (__any_sync(0xffffffffu, resc)) {
-            // rare: the running max rises; rescale l and this row of O once P V of
-            // the previous tile has landed in tensor memory
+            // rare: the running max rises; rescale l, and (low half) this row of O
+            // once P V of the previous tile has landed in tensor memory
             const float alpha = resc ? ex2(m - mn) : 1.f;
             l *= alpha;
-            if (!warp_wait(&p_free[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status)) { ok = false; break; }
-            tc_fence_after();
+            if (half == 0) {
+              if (!warp_wait(&p_free[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status)) { ok = false; break; }
+              tc_fence_after();
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              float o[32];
-              tc_ld32_sync(tl + c0, o);
+              for (int c0 = 0; c0 < D; c0 += 32) {
+                float o[32];
+                tc_ld32_sync(tl + c0, o);
 #pragma unroll
-              for (int q = 0; q < 32; ++q) o[q] *= alpha;
-              tc_st32(tl + c0, o);
+                for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                tc_st32(tl + c0, o);
+              }
+              tc_wait_st();
             }
-            tc_wait_st();
           }
           m = mn;
           // P of this tile goes to the buffer P V of tile i - 2 read
           if (i >= 2 && !warp_wait(&p_free[i & 1], ((i - 2) >> 1) & 1, p.status)) { ok = false; break; }
           if (is_row) {
-            uint32_t pk[TK / 2];
+            uint32_t pk[HK / 2];
             float ls = 0.f;
 #pragma unroll
-            for (int c = 0; c < TK; c += 2) {
+            for (int c = 0; c < HK; c += 2) {
               float p0 = ex2(fmaf(s[c], c2, -m)), p1 = ex2(fmaf(s[c + 1], c2, -m));
-              if (valid < TK) {
+              if (valid < HK) {
                 p0 = c < valid ? p0 : 0.f;
                 p1 = c + 1 < valid ? p1 : 0.f;
               }
@@ -403,22 +421,23 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
               pk[c / 2] = pack_bf16(p0, p1);
             }
             l += ls;
-            uint8_t* prow = sP + (i & 1) * C::P_BYTES + tid * 128;
+            uint8_t* prow = sP + (i & 1) * C::P_BYTES + row * 128;
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-              *reinterpret_cast<uint4*>(prow + ((cc ^ (tid & 7)) << 4)) =
+            for (int cc = 0; cc < HK / 8; ++cc)
+              *reinterpret_cast<uint4*>(prow + (((half * (HK / 8) + cc) ^ (row & 7)) << 4)) =
                   make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          } else if (is_sc) {
+          } else if (is_sc && valid > 0) {
             float* dst = p.part_s +
-                         (((static_cast<size_t>(sc_ms) * p.B + b) * p.Hkv + g) * 2 + sc_part) * p.s_stride + j * TK;
-            if (valid == TK) {
+                         (((static_cast<size_t>(sc_ms) * p.B + b) * p.Hkv + g) * 2 + sc_part) * p.s_stride + j * TK +
+                         half * HK;
+            if (valid >= HK) {
 #pragma unroll
-              for (int c = 0; c < TK; c += 4)
+              for (int c = 0; c < HK; c += 4)
                 *reinterpret_cast<float4*>(dst + c) =
                     make_float4(s[c] * p.scale, s[c + 1] * p.scale, s[c + 2] * p.scale, s[c + 3] * p.scale);
             } else {
 #pragma unroll
-              for (int c = 0; c < TK; ++c)
+              for (int c = 0; c < HK; ++c)
                 if (c < valid) dst[c] = s[c] * p.scale;
             }
           }
@@ -431,27 +450,33 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
       if (!ok) break;
       // run partial: (O, max, sum) of each query row once P V of its last tile landed
       const int last = i - 1;
-      if (!warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status)) break;
-      tc_fence_after();
-      if (32 * warp < p.M) {
-        const size_t prow = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g) * p.Mpad + tid;
-        float* orow = p.part_o + prow * D;
+      if (32 * quad < p.M) {  // the two halves' sums meet in the low half
+        if (half == 1) xl[row] = l;
+        named_bar(2 + quad, 64);
+      }
+      if (half == 0) {
+        if (!warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status)) break;
+        tc_fence_after();
+        if (32 * quad < p.M) {
+          const size_t prow = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g) * p.Mpad + row;
+          float* orow = p.part_o + prow * D;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float o[32];
-          tc_ld32_sync(tl + c0, o);
-          if (is_row) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float o[32];
+            tc_ld32_sync(tl + c0, o);
+            if (is_row) {
 #pragma unroll
-            for (int q = 0; q < 32; q += 4)
-              *reinterpret_cast<float4*>(orow + c0 + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+              for (int q = 0; q < 32; q += 4)
+                *reinterpret_cast<float4*>(orow + c0 + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+            }
+          }
+          if (is_row) {
+            p.part_ml[prow * 2 + 0] = m;
+            p.part_ml[prow * 2 + 1] = l + xl[row];
           }
         }
-        if (is_row) {
-          p.part_ml[prow * 2 + 0] = m;
-          p.part_ml[prow * 2 + 1] = l;
-        }
+        tc_fence_before();
       }
-      tc_fence_before();
       // next (sequence, KV head)
       j = 0;
       if (++g == p.Hkv) {
@@ -464,45 +489,53 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::RWARPS + 1) {
     tc_fence_after();
     tc_dealloc(tm, C::TMEM_COLS);
   }
 }
 
 // Merge of the partials with the verify rows' causal keys, output, append, scores.
-// Role A, one CTA per (sequence b, KV head g, verify row t): its G query rows.
-//   phase 1: every (segment, row) max/sum into shared memory (one round trip);
-//   phase 2: one warp per row, lanes across d, independent loads over segments.
-// Role B, one CTA per (sequence, 1024 positions): fixed-order sum of the per-KV-head
-// partial scores.
+// Role A, CTAs over (sequence b, KV head g, 8 consecutive rows r = t*G + jh of the
+// head's G*(gamma+1) query rows), one warp per row, lanes across d.  A warp issues
+// every load it needs in one round (the partials' max/sum, the first partial rows,
+// its query row and the verify rows' own keys and values u <= t), then merges in a
+// fixed order: partials by CTA, then the causal keys u = 0..t.
+// Role B, CTAs of 1024 prefix positions (4 per thread): fixed-order sum of the
+// per-(KV head, high / low part) partial scores.
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams p) {
-  extern __shared__ float cs[];                  // [nctas][G] max, [nctas][G] sum
-  __shared__ float lg[16][16];                   // [row in group][verify key u] logits, log2 units
-  __shared__ __align__(16) __nv_bfloat16 qs[16][D];  // this verify row's G query rows
-  __shared__ __align__(16) __nv_bfloat16 ks[16][D];  // the verify rows' own keys u <= t
-  __shared__ __align__(16) __nv_bfloat16 vs[16][D];  // ... and values
+__global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(const VerifyParams p) {
+  constexpr int PER = D / 32;  // elements of a row per lane
+  constexpr int NB = 8;        // partial rows per round of loads
+  __shared__ float lgs[kCombineWarps][16];               // a warp's causal logits (log2 units)
+  __shared__ __align__(16) __nv_bfloat16 kvs[2][16][D];  // the verify rows' keys and values
   pdl_wait();
   const int* cum = p.meta;
   const int* nlen = p.meta + p.B + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG = neg_inf();
-  const int nO = p.B * p.Hkv * p.R;
-  if (static_cast<int>(blockIdx.x) < nO) {
-    const int t = blockIdx.x % p.R;
-    const int bg = blockIdx.x / p.R;
+  const int rblocks = (p.M + kCombineWarps - 1) / kCombineWarps;  // CTAs per (sequence, KV head)
+  const int nA = p.B * p.Hkv * rblocks;
+  if (static_cast<int>(blockIdx.x) < nA) {
+    const int bg = blockIdx.x / rblocks;
+    const int r0 = (blockIdx.x - bg * rblocks) * kCombineWarps;
+    const int r = r0 + warp;  // row t*G + jh
     const int g = bg % p.Hkv, b = bg / p.Hkv;
     const int n = nlen[b];
-    if (n < 0) return;
+    if (n < 0) return;  // the whole CTA
     const int G = p.G;
+    const bool active = r < p.M;
+    const int t = active ? r / G : 0, jh = r - t * G;
+    const int tmax = min(p.M - 1, r0 + kCombineWarps - 1) / G;  // last verify row of this CTA
     const int64_t base = p.seq_offset[b];
+    const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
     const __nv_bfloat16* kn = p.k_new ? p.k_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
                                       : p.K + ((base + n) * p.Hkv + g) * D;
     const __nv_bfloat16* vn = p.v_new ? p.v_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
                                       : p.V + ((base + n) * p.Hkv + g) * D;
-    const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
-    // segments of this (sequence, KV head)
+    // partials of this (sequence, KV head): CTAs cf..cl of the verify split
     const int tiles = cum[b + 1] - cum[b];
     const int64_t T = static_cast<int64_t>(p.Hkv) * cum[p.B];
     int64_t cf = 0, cl = -1;
@@ -511,109 +544,156 @@ __global__ void __launch_bounds__(128) verify_combine_kernel(const VerifyParams 
       cf = owner_cta(S, T, p.nctas);
       cl = owner_cta(S + tiles - 1, T, p.nctas);
     }
-    const int nseg = static_cast<int>(cl - cf + 1);
+    const int nseg = active ? static_cast<int>(cl - cf + 1) : 0;
     const size_t pair = static_cast<size_t>(b) * p.Hkv + g;
-    float* cm = cs;
-    float* csum = cs + p.nctas * G;
-    // phase 1: one round of independent loads - each warp's partial output rows into
-    // registers, the verify rows' q/k/v and every partial's max/sum into shared memory
-    constexpr int NB = 16;
-    PartialRows<D, NB> pre;
-    const int jw = warp < G ? warp : 0;  // the row this warp merges first
-    auto orow = [&](int si) {
-      return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + t * G + jw) * D;
-    };
-    pre.load(orow, 0, 1, nseg, lane);
-    constexpr int CH = D / 8;  // 16-byte chunks per row
-    const __nv_bfloat16* qbase = p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G) * D;
-    for (int e = tid; e < G * CH; e += 128)
-      reinterpret_cast<uint4*>(&qs[0][0])[e] = reinterpret_cast<const uint4*>(qbase)[e];
-    for (int e = tid; e < (t + 1) * CH; e += 128) {
-      const int u = e / CH, c = e - u * CH;
-      reinterpret_cast<uint4*>(&ks[u][0])[c] = reinterpret_cast<const uint4*>(kn + u * row_stride)[c];
-      reinterpret_cast<uint4*>(&vs[u][0])[c] = reinterpret_cast<const uint4*>(vn + u * row_stride)[c];
-    }
-    for (int e = tid; e < nseg * G; e += 128) {
-      const int si = e / G, jh = e - si * G;
-      const int64_t c = cf + si;
-      float ms = NEG, ls = 0.f;
-      if (split_nonempty(c, T, p.nctas)) {  // CTAs with no items wrote no partial
-        const size_t r = (static_cast<size_t>(c) + pair) * p.Mpad + t * G + jh;
-        ms = p.part_ml[r * 2 + 0];
-        ls = p.part_ml[r * 2 + 1];
+    auto prow = [&](int si) { return (static_cast<size_t>(cf + si) + pair) * p.Mpad + r; };
+    auto load_ml = [&](int si, float& ms, float& ls) {
+      ms = NEG;
+      ls = 0.f;
+      if (si < nseg && split_nonempty(cf + si, T, p.nctas)) {  // CTAs with no items wrote no partial
+        const float2 v = *reinterpret_cast<const float2*>(p.part_ml + prow(si) * 2);
+        ms = v.x;
+        ls = v.y;
       }
-      cm[si * G + jh] = ms;
-      csum[si * G + jh] = ls;
+    };
+    auto load_rows = [&](int s0, float (&v)[NB][PER]) {
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        const int si = s0 + q < nseg ? s0 + q : 0;  // a readable row; unused if past nseg
+        const float* src = p.part_o + prow(si) * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          v[q][0] = x.x; v[q][1] = x.y;
+        }
+      }
+    };
+    // ---- one round of loads: the verify rows' keys/values (the CTA, into shared
+    // memory), this warp's partial max/sum, first two batches of partial rows, query
+    constexpr int CH = D / 8;  // 16-byte chunks of a row
+    for (int e = tid; e < 2 * (tmax + 1) * CH; e += kCombineWarps * 32) {
+      const int which = e / ((tmax + 1) * CH), rem = e - which * (tmax + 1) * CH;
+      const int u = rem / CH, c = rem - u * CH;
+      reinterpret_cast<uint4*>(&kvs[which][u][0])[c] =
+          reinterpret_cast<const uint4*>((which ? vn : kn) + u * row_stride)[c];
+    }
+    float pm = NEG, pl = 0.f;
+    float va[NB][PER], vb[NB][PER];
+    float qv[PER];
+    if (active) {
+      load_ml(lane, pm, pl);
+      load_rows(0, va);
+      load_rows(NB, vb);
+      const __nv_bfloat16* qrow = p.q + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) qv[e] = bf2f(qrow[e]);
     }
     __syncthreads();
-    // logits of the verify rows' own keys u <= t (causal), from shared memory
-    for (int pr = warp; pr < G * (t + 1); pr += 4) {
-      const int jh = pr / (t + 1), u = pr - jh * (t + 1);
+    if (!active) return;
+    // ---- causal logits of the verify rows' own keys u <= t
+    float* lg = lgs[warp];
+    float mc = NEG;
+    for (int u = 0; u <= t; ++u) {
       float acc = 0.f;
-      for (int e = lane; e < D; e += 32) acc += bf2f(qs[jh][e]) * bf2f(ks[u][e]);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc += qv[e] * bf2f(kvs[0][u][lane * PER + e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0) lg[jh][u] = acc * p.scale_log2;
+      acc *= p.scale_log2;
+      mc = fmaxf(mc, acc);
+      if (lane == 0) lg[u] = acc;
     }
-    __syncthreads();
-    // phase 2: one warp per query row, lanes across d
-    constexpr int PER = D / 32;
-    for (int jh = warp; jh < G; jh += 4) {
-      float M = NEG;
-      for (int si = lane; si < nseg; si += 32) M = fmaxf(M, cm[si * G + jh]);
-      for (int u = lane; u <= t; u += 32) M = fmaxf(M, lg[jh][u]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float acc[PER];
-#pragma unroll
-      for (int q = 0; q < PER; ++q) acc[q] = 0.f;
-      float l = 0.f;
-      const int m = t * G + jh;
-      auto orow_j = [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + pair) * p.Mpad + m) * D; };
-      if (jh == warp) {  // first row of this warp: most partials are already in registers
-        pre.accumulate(cm + jh, csum + jh, G, 0, 1, nseg, M, acc, l);
-        merge_partials<D>(cm + jh, csum + jh, G, nseg, M, orow_j, acc, l, lane, NB, 1);
-      } else {
-        merge_partials<D>(cm + jh, csum + jh, G, nseg, M, orow_j, acc, l, lane);
-      }
-      for (int u = 0; u <= t; ++u) {
-        const float w = ex2(lg[jh][u] - M);
-        l += w;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) acc[q] += w * bf2f(vs[u][lane * PER + q]);
-      }
-      const float inv = 1.f / l;
-      __nv_bfloat16* o = p.out + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + lane * PER;
-#pragma unroll
-      for (int q = 0; q < PER; ++q) o[q] = __float2bfloat16_rn(acc[q] * inv);
+    __syncwarp();
+    // ---- global max over the partials and the causal keys
+    float M = pm;
+    for (int s0 = 32; s0 < nseg; s0 += 32) {  // more than 32 partials: further rounds
+      float ms, ls;
+      load_ml(s0 + lane, ms, ls);
+      M = fmaxf(M, ms);
     }
-    if (p.k_new) {  // append verify row t (the chain enters the cache)
-      const size_t dst = ((base + n + t) * p.Hkv + g) * D;
-      for (int c = tid; c < CH; c += 128) {
-        reinterpret_cast<uint4*>(p.K + dst)[c] = reinterpret_cast<const uint4*>(&ks[t][0])[c];
-        reinterpret_cast<uint4*>(p.V + dst)[c] = reinterpret_cast<const uint4*>(&vs[t][0])[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    M = fmaxf(M, mc);
+    // ---- merge, in the order of the partials, then the causal keys; two batches of
+    // partial rows in flight (the next is loaded while this one is added)
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float l = 0.f, w = 0.f;
+    for (int s0 = 0; s0 < nseg; s0 += NB) {
+      if ((s0 & 31) == 0) {  // weights of the next 32 partials
+        float ms = pm, ls = pl;
+        if (s0 > 0) load_ml(s0 + lane, ms, ls);
+        w = (ms != NEG) ? ex2(ms - M) : 0.f;
+        float wl = w * ls;  // fixed-order butterfly
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, off);
+        l += wl;
+      }
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        const float wq = __shfl_sync(0xffffffffu, w, (s0 + q) & 31);
+        if (s0 + q < nseg) {
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] += wq * va[q][e];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NB; ++q)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) va[q][e] = vb[q][e];
+      if (s0 + 2 * NB < nseg) load_rows(s0 + 2 * NB, vb);
+    }
+    for (int u = 0; u <= t; ++u) {
+      const float wu = ex2(lg[u] - M);
+      l += wu;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += wu * bf2f(kvs[1][u][lane * PER + e]);
+    }
+    const float inv = 1.f / l;
+    __nv_bfloat16* o = p.out + ((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = __float2bfloat16_rn(acc[e] * inv);
+    if (p.k_new && jh == 0) {  // append verify row t (the chain enters the cache)
+      const size_t dst = ((base + n + t) * p.Hkv + g) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        p.K[dst + e] = kvs[0][t][lane * PER + e];
+        p.V[dst + e] = kvs[1][t][lane * PER + e];
       }
     }
     return;
   }
-  // score role: fixed-order sum of the per-KV-head partial scores
-  const int nchunks = (p.max_len + kScoreChunk - 1) / kScoreChunk;
-  const int sb = blockIdx.x - nO;
+  // score role: fixed-order sum of the per-(KV head, part) partial scores
+  constexpr int CH = kCombineWarps * 32 * 4;
+  const int nchunks = (p.max_len + CH - 1) / CH;
+  const int sb = blockIdx.x - nA;
   const int b = sb / nchunks, ch = sb - b * nchunks;
   if (b >= p.B) return;
   const int n = nlen[b];
-  const int lo = ch * kScoreChunk, hi = min(n, lo + kScoreChunk);
+  const int pos = ch * CH + tid * 4;
+  if (pos >= n) return;
+  const int parts = p.Hkv * 2;
   for (int ms = 0; ms < 2; ++ms) {
     float* dst = ms ? p.scores1 : p.scores0;
     if ((ms ? p.mask1 : p.mask0) == 0u || dst == nullptr) continue;
-    const int parts = p.Hkv * 2;  // (KV head, high / low part) shares, in a fixed order
-    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.s_stride;
-    for (int pos = lo + tid; pos < hi; pos += 128) {
-      float v = 0.f;
+    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.s_stride + pos;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-      for (int q = 0; q < parts; ++q) v += src[static_cast<size_t>(q) * p.s_stride + pos];
-      dst[static_cast<size_t>(b) * p.score_stride + pos] = v;
+    for (int q = 0; q < parts; ++q) {  // rows are s_stride (a multiple of 64) apart: in bounds
+      const float4 v = *reinterpret_cast<const float4*>(src + static_cast<size_t>(q) * p.s_stride);
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
     }
+    float* d = dst + static_cast<size_t>(b) * p.score_stride + pos;
+    d[0] = a.x;
+    if (pos + 1 < n) d[1] = a.y;
+    if (pos + 2 < n) d[2] = a.z;
+    if (pos + 3 < n) d[3] = a.w;
   }
 }
 
@@ -637,12 +717,13 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
     }
     return e;
   }
-  const int nO = p.B * p.Hkv * p.R;
-  const int nS = ((p.mask0 | p.mask1) != 0u) ? p.B * ((p.max_len + kScoreChunk - 1) / kScoreChunk) : 0;
+  const int nA = p.B * p.Hkv * ((p.M + kCombineWarps - 1) / kCombineWarps);
+  constexpr int CH = kCombineWarps * 32 * 4;
+  const int nS = ((p.mask0 | p.mask1) != 0u) ? p.B * ((p.max_len + CH - 1) / CH) : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nO + nS);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = static_cast<size_t>(p.nctas) * p.G * 2 * sizeof(float);
+  cfg.gridDim = dim3(nA + nS);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -12,8 +12,6 @@ namespace vg {
 
 // Keys per verify tile: the unit of TMA transfer and of the work split.
 constexpr int kVerifyTileKeys = 64;
-// Prefix positions per score-reduction block of the verify combine kernel (one per thread).
-constexpr int kScoreChunk = 128;
 // Longest draft-token tail a sparse draft step attends besides the selection.
 constexpr int kDraftMaxTail = 64;
 // Largest sequence the top-k kernel holds in shared memory across a cluster of 8.
