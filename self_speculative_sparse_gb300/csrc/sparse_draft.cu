@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kKeys = 16;  // entries per pipeline stage
 constexpr int kStages = 2;
-constexpr int kCombineWarps = 8;
+constexpr int kCombineRows = 12;  // partial rows a combine warp loads in its first round
 
 struct DLayout {
   int row;  // bytes per gathered page in shared memory (padded by 16: ldmatrix rows hit distinct banks)
@@ -80,7 +80,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   const int x1 = static_cast<int>(split_begin(blockIdx.x + 1, E, p.nctas));
   pdl_launch_dependents();
   if (x0 >= x1) return;
-  pdl_wait();  // idx / count come from the selection kernel
+  // idx / count come from the selection kernel, the tail pages from the previous step.
+  // Kernels of this library trigger their dependents early, so several may be in
+  // flight: nothing an earlier kernel writes is read before this wait.
+  pdl_wait();
   const int page = p.Hkv * D * 2;  // bytes of one token's K (or V), all heads
 
   // ------------------------------------------------------------ producer warp
@@ -231,13 +234,15 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   }
 }
 
-// One CTA per (query head h, sequence b).  Phase 1 loads every partial's max/sum
-// in one round trip; phase 2 splits the partials over 8 warps (lanes across d,
-// batched independent loads) and sums the warps' results in a fixed order.  The
-// CTA of each KV head's first query head then appends the current draft token.
-template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32) draft_combine_kernel(const DraftParams p) {
-  extern __shared__ float cs[];  // [nctas] max, [nctas] sum
+// One CTA per (query head h, sequence b), NW warps (enough that each holds at most
+// kCombineRows partials).  Warp w owns partials w, w + NW, ...: it loads their (max, sum) one per lane and their output rows (lanes across d)
+// in a single round, the CTA agrees on the global max through shared memory, and the
+// warps' weighted sums are added in a fixed order (deterministic).  The CTA of each
+// KV head's first query head then appends the current draft token.
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParams p) {
+  constexpr int kCombineWarps = NW;
+  constexpr int PER = D / 32;  // elements of a row per lane
   __shared__ float red[kCombineWarps][D];
   __shared__ float redl[kCombineWarps];
   __shared__ float redm[kCombineWarps];
@@ -250,46 +255,67 @@ __global__ void __launch_bounds__(kCombineWarps * 32) draft_combine_kernel(const
   const int64_t E = static_cast<int64_t>(p.B) * S;
   const int64_t cf = owner_cta(static_cast<int64_t>(b) * S, E, p.nctas);
   const int64_t cl = owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, p.nctas);
-  const int nseg = static_cast<int>(cl - cf + 1);
+  const int nseg = static_cast<int>(cl - cf + 1);  // <= 32 * kCombineWarps (host choice)
+  auto prow = [&](int si) { return (static_cast<size_t>(cf + si) + b) * p.Hq + h; };
+  pdl_launch_dependents();  // the next draft step may start its prologue
   pdl_wait();
-  float* cm = cs;
-  float* csum = cs + p.nctas;
-  // each warp's share of the partial output rows goes to registers first, so these
-  // loads overlap those of the maxima and sums
-  constexpr int NB = 16;
-  auto orow = [&](int si) { return p.part_o + ((static_cast<size_t>(cf + si) + b) * p.Hq + h) * D; };
-  PartialRows<D, NB> pre;
-  pre.load(orow, warp, kCombineWarps, nseg, lane);
-  for (int si = tid; si < nseg; si += kCombineWarps * 32) {
-    const int64_t c = cf + si;
-    float ms = NEG, ls = 0.f;
-    if (split_nonempty(c, E, p.nctas)) {  // CTAs with no entries wrote no partial
-      const size_t r = (static_cast<size_t>(c) + b) * p.Hq + h;
-      ms = p.part_ml[r * 2 + 0];
-      ls = p.part_ml[r * 2 + 1];
+  // ---- one round of loads: lane q holds (max, sum) of partial warp + NW q; the first
+  // kCombineRows output rows of the warp's partials go to registers
+  float pm = NEG, pl = 0.f;
+  {
+    const int si = warp + kCombineWarps * lane;
+    if (si < nseg && split_nonempty(cf + si, E, p.nctas)) {  // CTAs with no entries wrote no partial
+      const float2 v = *reinterpret_cast<const float2*>(p.part_ml + prow(si) * 2);
+      pm = v.x;
+      pl = v.y;
     }
-    cm[si] = ms;
-    csum[si] = ls;
   }
+  float v[kCombineRows][PER];
+#pragma unroll
+  for (int q = 0; q < kCombineRows; ++q) {
+    const int si = warp + kCombineWarps * q;
+    const float* src = p.part_o + prow(si < nseg ? si : 0) * D + lane * PER;  // a readable row
+    if constexpr (PER == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(src);
+      v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(src);
+      v[q][0] = x.x; v[q][1] = x.y;
+    }
+  }
+  // ---- global max
+  float mx = pm;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) redm[warp] = mx;
   __syncthreads();
   float M = NEG;
-  for (int si = tid; si < nseg; si += kCombineWarps * 32) M = fmaxf(M, cm[si]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) redm[warp] = M;
-  __syncthreads();
-  M = NEG;
 #pragma unroll
   for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, redm[w]);
-  constexpr int PER = D / 32;
+  // ---- this warp's weighted sum, partials in order
+  const float wt = (pm != NEG) ? ex2(pm - M) : 0.f;
+  float l = wt * pl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   float acc[PER];
 #pragma unroll
-  for (int q = 0; q < PER; ++q) acc[q] = 0.f;
-  float l = 0.f;
-  pre.accumulate(cm, csum, 1, warp, kCombineWarps, nseg, M, acc, l);
-  merge_partials<D>(cm, csum, 1, nseg, M, orow, acc, l, lane, warp + NB * kCombineWarps, kCombineWarps);
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll
-  for (int q = 0; q < PER; ++q) red[warp][lane * PER + q] = acc[q];
+  for (int q = 0; q < kCombineRows; ++q) {
+    const float wq = __shfl_sync(0xffffffffu, wt, q);
+    if (warp + kCombineWarps * q < nseg) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += wq * v[q][e];
+    }
+  }
+  for (int q = kCombineRows; warp + kCombineWarps * q < nseg; ++q) {  // rare: more partials per warp
+    const float wq = __shfl_sync(0xffffffffu, wt, q);
+    const float* src = p.part_o + prow(warp + kCombineWarps * q) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += wq * src[e];
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) red[warp][lane * PER + e] = acc[e];
   if (lane == 0) redl[warp] = l;
   __syncthreads();
   if (tid < D) {
@@ -333,14 +359,30 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
   cfg.numAttrs = pdl ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW>, p);
   if (e != cudaSuccess) return e;
+  // partials per sequence: the CTAs whose static ranges meet its slots
+  const int64_t E = static_cast<int64_t>(p.B) * draft_slots(p);
+  int nseg_max = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int64_t cf = owner_cta(static_cast<int64_t>(b) * draft_slots(p), E, p.nctas);
+    const int64_t cl = owner_cta(static_cast<int64_t>(b + 1) * draft_slots(p) - 1, E, p.nctas);
+    nseg_max = max(nseg_max, static_cast<int>(cl - cf + 1));
+  }
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(p.Hq, p.B);
-  cfg2.blockDim = dim3(kCombineWarps * 32);
-  cfg2.dynamicSmemBytes = static_cast<size_t>(p.nctas) * 2 * sizeof(float);
+  cfg2.dynamicSmemBytes = 0;
   cfg2.stream = stream;
   cfg2.attrs = at;
   cfg2.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D>, p);
+  if (nseg_max <= 4 * kCombineRows) {
+    cfg2.blockDim = dim3(4 * 32);
+    return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 4>, p);
+  }
+  if (nseg_max <= 8 * kCombineRows) {
+    cfg2.blockDim = dim3(8 * 32);
+    return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 8>, p);
+  }
+  cfg2.blockDim = dim3(16 * 32);
+  return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 16>, p);
 }
 
 }  // namespace

@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31;
 
+  pdl_launch_dependents();  // the draft step may start its prologue
   pdl_wait();
   int n = p.len[b];
   if (n < 0 || n > p.max_len || n > C * p.per_cta) {

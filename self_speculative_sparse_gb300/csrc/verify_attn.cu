@@ -511,6 +511,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
   constexpr int NB = 8;        // partial rows per round of loads
   __shared__ float lgs[kCombineWarps][16];               // a warp's causal logits (log2 units)
   __shared__ __align__(16) __nv_bfloat16 kvs[2][16][D];  // the verify rows' keys and values
+  pdl_launch_dependents();  // the selection kernel may start its prologue
   pdl_wait();
   const int* cum = p.meta;
   const int* nlen = p.meta + p.B + 1;

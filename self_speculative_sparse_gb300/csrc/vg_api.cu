@@ -360,7 +360,7 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.D = s.D;
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
-  p.nctas = di.sms;
+  p.nctas = di.sms < 512 ? di.sms : 512;  // the combine gathers a sequence's partials in one round (<= 512)
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);
   p.out = static_cast<__nv_bfloat16*>(a.out);
