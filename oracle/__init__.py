@@ -14,6 +14,7 @@ from .vegas import (  # noqa: F401
     verify_attention,
     verify_logits,
     aggregated_scores,
+    aggregated_scores_grouped,
     select_topk,
     sparse_draft_attention,
     draft_step,

@@ -130,6 +130,26 @@ def aggregated_scores(q: np.ndarray, K: np.ndarray, rows, scale: float | None = 
     return L[rows].sum(axis=(0, 1))
 
 
+def aggregated_scores_grouped(q: np.ndarray, K: np.ndarray, rows, scale: float | None = None) -> np.ndarray:
+    """The per-entry objective of aggregated_scores, computed through the linearity of
+    the dot product: summed over the rows and the query heads of KV head g, the logits
+    of entry i equal scale * k_{i,g} . (the sum of those query vectors).  One n x d
+    product per KV head instead of one per (row, query head); the full-size checks
+    use it.  [n]."""
+    R, Hq, d = q.shape
+    n, Hkv, _ = K.shape
+    s = _default_scale(d, scale)
+    G, _ = _heads(Hq, Hkv)
+    rows = sorted(set(int(t) for t in rows))
+    if any(t < 0 or t >= R for t in rows):
+        raise ValueError("row outside the verify chain")
+    out = np.zeros(n)
+    for g in range(Hkv):
+        qsum = q[rows][:, g * G:(g + 1) * G, :].sum(axis=(0, 1))
+        out += K[:, g, :] @ qsum
+    return out * s
+
+
 def select_topk(s: np.ndarray, k: int) -> np.ndarray:
     """The size-k subset maximising Σ_{i in T} s_i (Vegas §2.A's argmax).
 

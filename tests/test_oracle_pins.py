@@ -212,6 +212,9 @@ def test_scores_linearity_identity(rows):
     a = oracle.aggregated_scores(q, K, rows)
     b = _linearity_scores(q, K, rows, 1.0 / math.sqrt(d))
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12 * np.abs(b).max())
+    # the oracle's grouped form (used at full size) is the same identity
+    c = oracle.aggregated_scores_grouped(q, K, rows)
+    np.testing.assert_allclose(c, a, rtol=1e-12, atol=1e-12 * np.abs(a).max())
 
 
 def test_collect2_equals_all_rows_when_gamma_is_one():
