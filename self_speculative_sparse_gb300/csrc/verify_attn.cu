@@ -9,11 +9,13 @@
 //
 // GB300 design.  The work is the flattened list of (sequence, KV head, 64-key tile)
 // items, split evenly over one persistent CTA per SM (ragged batches balance by
-// construction).  Each CTA runs three roles:
+// construction).  Each CTA runs four roles:
 //   warp 8   streams K and V tiles by 2-D TMA (128-byte swizzle) into a ring of
 //            shared-memory stages;
 //   warp 9   issues tcgen05.mma from one thread: S = Q K^T into a double-buffered
-//            tensor-memory tile, then O += P V into a tensor-memory accumulator;
+//            tensor-memory tile;
+//   warp 10  issues O += P V from one thread into a tensor-memory accumulator, as
+//            soon as a tile's P is written;
 //   warps 0-7 own the 128 tensor-memory lanes, one A-operand row per lane: the
 //            G*(gamma+1) query rows of the current KV head, then two rows per score
 //            mask that hold the mask's summed query split into a bf16 high and low
@@ -23,7 +25,9 @@
 // sum are per thread; the two halves of a row agree on the tile max through shared
 // memory; the running max is raised only when a tile exceeds it by more than 2^8,
 // after which the row's O is rescaled in tensor memory), and writes its half row of
-// P (bf16) to shared memory for the P V product.  A score-row
+// P (bf16) to shared memory for the P V product.  When the query and score rows fit in
+// 64, the MMAs use M = 64, which halves the Q and P buffers and leaves room for a fifth
+// stage.  A score-row
 // thread's S row is already the summed logit q_sum . k of each key of the tile
 // (high part plus low part), so the aggregation costs two rows of the same MMA and
 // no shuffles; the cache is read exactly once.  Each contiguous run of tiles of one
@@ -46,25 +50,31 @@ constexpr int TK = kVerifyTileKeys;
 // (log2 units), so P stays below 2^8 and rescaling O is rare.
 constexpr float kRescaleSlack = 8.f;
 
-template <int D>
+// MR: rows of the MMA (64 when the query and score rows fit, else 128).  With
+// M = 64 the accumulator's row r sits in lane 16 (r / 16) + r % 16 of quadrant r / 16.
+template <int D, int MR>
 struct TCfg {
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int STAGE_BYTES_ = 2 * kVerifyTileKeys * D * 2;
+  static constexpr int kStages =  // as many stages as 192 KB leave beside Q and two P buffers
+      (196608 - (D / 64) * MR * 128 - 2 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_ > 12
+          ? 12
+          : (196608 - (D / 64) * MR * 128 - 2 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_;
   static constexpr int HALVES = D / 64;             // 64-column (128-byte) swizzled boxes
   static constexpr int HALF_BYTES = TK * 128;       // one box of a K or V tile
   static constexpr int TILE_BYTES = TK * D * 2;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile, then V tile
-  static constexpr int QHALF = 128 * 128;           // A operand: 128 rows x 64 columns
-  static constexpr int P_BYTES = 128 * TK * 2;      // P: 128 rows x 64 keys (one box wide)
+  static constexpr int QHALF = MR * 128;            // A operand: MR rows x 64 columns
+  static constexpr int P_BYTES = MR * TK * 2;       // P: MR rows x 64 keys (one box wide)
   static constexpr int OFF_Q = kStages * STAGE_BYTES;
   static constexpr int OFF_P = OFF_Q + HALVES * QHALF;  // two P buffers
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin
-  static constexpr int NBAR = 2 * kStages + 10;
+  // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin[2]
+  static constexpr int NBAR = 2 * kStages + 11;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_X = OFF_TMEM + 16;       // float xm[2][2][128] tile maxima, xl[128] sums
   static constexpr int OFF_META = OFF_X + 5 * 128 * 4;  // int cum[B+1], nlen[B]
   static constexpr int RWARPS = 8;                  // row warps: two per tensor-memory lane quadrant
-  static constexpr int THREADS = (RWARPS + 2) * 32; // + TMA producer warp + MMA warp
+  static constexpr int THREADS = (RWARPS + 3) * 32; // + TMA producer, Q K^T issuer, P V issuer
   static constexpr uint32_t TMEM_COLS = 256;        // O at columns [0, D), S buffers at 128 and 192
   static constexpr uint32_t COL_S = 128;
   static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
@@ -135,11 +145,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
 }
 
-template <int D>
-__global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
+template <int D, int MR>
+__global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  using C = TCfg<D>;
+  using C = TCfg<D, MR>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,19 +184,20 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
       mbar_init(&p_free[s], 1);
     }
     mbar_init(q_ready, C::RWARPS);
-    mbar_init(fin, 1);
+    mbar_init(&fin[0], 1);
+    mbar_init(&fin[1], 1);
     fence_mbar_init();
   }
-  if (warp == C::RWARPS + 1) tc_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == C::RWARPS + 1) tc_alloc(tmem_slot, C::TMEM_COLS);  // (and frees it at the end)
   // A-operand rows no segment writes stay zero: Q rows >= arows, P rows >= M
   {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    const int qz = (128 - arows) * 8;
+    const int qz = (MR - arows) * 8;
     for (int e = threadIdx.x; e < C::HALVES * qz; e += C::THREADS) {
       const int h = e / qz, r = arows + (e - h * qz) / 8, c = e & 7;
       *reinterpret_cast<uint4*>(sQ + h * C::QHALF + r * 128 + c * 16) = z;
     }
-    const int pz = (128 - p.M) * 8;
+    const int pz = (MR - p.M) * 8;
     for (int e = threadIdx.x; e < 2 * pz; e += C::THREADS) {
       const int buf = e / pz, r = p.M + (e - buf * pz) / 8, c = e & 7;
       *reinterpret_cast<uint4*>(sP + buf * C::P_BYTES + r * 128 + c * 16) = z;
@@ -232,39 +243,20 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
     // no copy may still be in flight when the CTA exits (normally all were consumed)
     for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
   } else if (ntiles > 0 && warp == C::RWARPS + 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idS = tc_idesc_bf16(128, TK, 0, 0);
-    constexpr uint32_t idO = tc_idesc_bf16(128, D, 0, 1);
-    const uint32_t base = smem_u32(smem), qaddr = smem_u32(sQ), paddr = smem_u32(sP);
-    // O += P V for tile x (first: the first tile of its run, which overwrites O)
-    auto pv = [&](int x, bool first) -> bool {
-      if (!mbar_wait(&p_full[x & 1], (x >> 1) & 1, p.status)) return false;
-      tc_fence_after();
-      const int st = x % S;
-      const uint32_t vaddr = base + st * C::STAGE_BYTES + C::TILE_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < TK / 16; ++kk)
-        tc_mma(tm, tc_desc_sw128(paddr + (x & 1) * C::P_BYTES + kk * 32, 16, 1024),
-               tc_desc_sw128(vaddr + kk * 2048, C::HALF_BYTES, 1024), idO, (kk > 0 || !first) ? 1u : 0u);
-      tc_commit(&empty[st]);
-      tc_commit(&p_free[x & 1]);
-      return true;
-    };
+    // ---------------------------------------------------------------- Q K^T issuer
+    constexpr uint32_t idS = tc_idesc_bf16(MR, TK, 0, 0);
+    const uint32_t base = smem_u32(smem), qaddr = smem_u32(sQ);
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
     int seg = 0;
-    bool prev_first = false, ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      const bool first = (i == 0) || (j == 0);
-      // at a run boundary the row warps read O only after the previous run's last P V
-      if (i > 0 && first && !pv(i - 1, prev_first)) { ok = false; break; }
-      if (first) {
-        if (!mbar_wait(q_ready, seg & 1, p.status)) { ok = false; break; }
+    for (int i = 0; i < ntiles; ++i) {
+      if (i == 0 || j == 0) {  // a new run: its query rows must be in shared memory
+        if (!mbar_wait(q_ready, seg & 1, p.status)) break;
         ++seg;
       }
       const int st = i % S;
-      if (!mbar_wait(&full[st], (i / S) & 1, p.status)) { ok = false; break; }
-      if (i >= 2 && !mbar_wait(&s_free[i & 1], ((i - 2) >> 1) & 1, p.status)) { ok = false; break; }
+      if (!mbar_wait(&full[st], (i / S) & 1, p.status)) break;
+      if (i >= 2 && !mbar_wait(&s_free[i & 1], ((i - 2) >> 1) & 1, p.status)) break;
       tc_fence_after();
       const uint32_t kaddr = base + st * C::STAGE_BYTES;
 #pragma unroll
@@ -274,24 +266,45 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
                tc_desc_sw128(kaddr + (kk >> 2) * C::HALF_BYTES + (kk & 3) * 32, 16, 1024), idS,
                kk > 0 ? 1u : 0u);
       tc_commit(&s_full[i & 1]);
-      // steady state: the previous tile's P V goes after this tile's Q K^T, so the
-      // row warps find S ready as soon as they finish P
-      if (i > 0 && !first && !pv(i - 1, prev_first)) { ok = false; break; }
-      prev_first = first;
       advance(b, g, j, cum, p.B, p.Hkv);
     }
-    if (ok) pv(ntiles - 1, prev_first);
-    tc_commit(fin);  // every MMA of this thread complete before the CTA tears down
-    mbar_wait(fin, 0, p.status);
+    tc_commit(&fin[0]);  // every MMA of this thread complete before the CTA tears down
+    mbar_wait(&fin[0], 0, p.status);
+  } else if (ntiles > 0 && warp == C::RWARPS + 2 && lane == 0) {
+    // ---------------------------------------------------------------- P V issuer
+    // (its own thread, so P V of a tile starts as soon as P is written, not after the
+    // next tile's Q K^T has been issued)
+    constexpr uint32_t idO = tc_idesc_bf16(MR, D, 0, 1);
+    const uint32_t base = smem_u32(smem), paddr = smem_u32(sP);
+    int b, g, j;
+    locate(t0, cum, p.B, p.Hkv, b, g, j);
+    for (int i = 0; i < ntiles; ++i) {
+      const bool first = (i == 0) || (j == 0);  // the first tile of a run overwrites O
+      if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, p.status)) break;
+      tc_fence_after();
+      const int st = i % S;
+      const uint32_t vaddr = base + st * C::STAGE_BYTES + C::TILE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < TK / 16; ++kk)
+        tc_mma(tm, tc_desc_sw128(paddr + (i & 1) * C::P_BYTES + kk * 32, 16, 1024),
+               tc_desc_sw128(vaddr + kk * 2048, C::HALF_BYTES, 1024), idO, (kk > 0 || !first) ? 1u : 0u);
+      tc_commit(&empty[st]);
+      tc_commit(&p_free[i & 1]);
+      advance(b, g, j, cum, p.B, p.Hkv);
+    }
+    tc_commit(&fin[1]);
+    mbar_wait(&fin[1], 0, p.status);
   } else if (ntiles > 0 && warp < C::RWARPS) {
     // ---------------------------------------------------------------- row warps
     constexpr int NR = C::RWARPS * 32;
     constexpr int HK = TK / 2;            // keys of a tile per half
     const int rtid = threadIdx.x;         // 0 .. NR-1, for cooperative loops
     const int quad = warp & 3, half = warp >> 2;
-    const int row = 32 * quad + lane;     // = tensor-memory lane = A-operand row
+    constexpr int QR = MR / 4;            // accumulator rows per lane quadrant
+    const int row = lane < QR ? QR * quad + lane : 128;  // A-operand row of this lane (128: none)
+    const bool has_row = row < 128;
     const uint32_t tl = tm + (static_cast<uint32_t>(32 * quad) << 16);
-    const bool wact = 32 * quad < arows;  // warp-uniform: lanes hold rows in use
+    const bool wact = QR * quad < arows;  // warp-uniform: lanes hold rows in use
     const bool is_row = row < p.M;
     const int sci = row - p.M;
     const bool is_sc = sci >= 0 && sci < nsc;
@@ -379,9 +392,9 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
           }
           mx *= c2;
           // both halves of the row take the max of the whole tile
-          xm[((i & 1) * 2 + half) * 128 + row] = mx;
+          if (has_row) xm[((i & 1) * 2 + half) * 128 + row] = mx;
           named_bar(2 + quad, 64);
-          mx = fmaxf(mx, xm[((i & 1) * 2 + (half ^ 1)) * 128 + row]);
+          if (has_row) mx = fmaxf(mx, xm[((i & 1) * 2 + (half ^ 1)) * 128 + row]);
           const bool first = (i == seg_first);
           const float mn = (is_row && (first || mx > m + kRescaleSlack)) ? fmaxf(m, mx) : m;
           const bool resc = is_row && !first && mn != m;
@@ -450,14 +463,14 @@ __global__ void __launch_bounds__(TCfg<D>::THREADS, 1)
       if (!ok) break;
       // run partial: (O, max, sum) of each query row once P V of its last tile landed
       const int last = i - 1;
-      if (32 * quad < p.M) {  // the two halves' sums meet in the low half
-        if (half == 1) xl[row] = l;
+      if (QR * quad < p.M) {  // the two halves' sums meet in the low half
+        if (half == 1 && has_row) xl[row] = l;
         named_bar(2 + quad, 64);
       }
       if (half == 0) {
         if (!warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status)) break;
         tc_fence_after();
-        if (32 * quad < p.M) {
+        if (QR * quad < p.M) {
           const size_t prow = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g) * p.Mpad + row;
           float* orow = p.part_o + prow * D;
 #pragma unroll 1
@@ -698,22 +711,22 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
   }
 }
 
-template <int D>
+template <int D, int MR>
 cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             cudaStream_t stream) {
-  using C = TCfg<D>;
+  using C = TCfg<D, MR>;
   const size_t smem = C::smem(p.B);
-  cudaError_t e = ensure_smem<verify_kernel<D>>(smem);
+  cudaError_t e = ensure_smem<verify_kernel<D, MR>>(smem);
   if (e != cudaSuccess) return e;
-  verify_kernel<D><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
+  verify_kernel<D, MR><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, verify_kernel<D>) == cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, verify_kernel<D, MR>) == cudaSuccess) {
       fprintf(stderr,
-              "verify_kernel<%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
+              "verify_kernel<%d,%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
               "requestedSmem=%zu localBytes=%zu)\n",
-              D, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, C::THREADS, fa.sharedSizeBytes,
+              D, MR, cudaGetErrorString(e), fa.numRegs, fa.maxThreadsPerBlock, C::THREADS, fa.sharedSizeBytes,
               fa.maxDynamicSharedSizeBytes, smem, fa.localSizeBytes);
     }
     return e;
@@ -737,15 +750,23 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
 }  // namespace
 
 size_t verify_smem_bytes(int D, int B) {
-  if (D == 64) return TCfg<64>::smem(B);
-  if (D == 128) return TCfg<128>::smem(B);
+  auto mx = [](size_t a, size_t b) { return a > b ? a : b; };
+  if (D == 64) return mx(TCfg<64, 64>::smem(B), TCfg<64, 128>::smem(B));
+  if (D == 128) return mx(TCfg<128, 64>::smem(B), TCfg<128, 128>::smem(B));
   return 0;
 }
 
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream) {
-  if (p.D == 64) return launch_verify_t<64>(p, tmK, tmV, stream);
-  if (p.D == 128) return launch_verify_t<128>(p, tmK, tmV, stream);
+  // A-operand rows: the query rows, then a high and a low row per score mask
+  const int arows = p.M + 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));
+  if (arows <= 64) {
+    if (p.D == 64) return launch_verify_t<64, 64>(p, tmK, tmV, stream);
+    if (p.D == 128) return launch_verify_t<128, 64>(p, tmK, tmV, stream);
+  } else {
+    if (p.D == 64) return launch_verify_t<64, 128>(p, tmK, tmV, stream);
+    if (p.D == 128) return launch_verify_t<128, 128>(p, tmK, tmV, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
