@@ -30,6 +30,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;  // radix digit: 8 bits
+constexpr int kListPerWarp = 256;  // candidate-list capacity of a warp for the last two passes
 
 // fp32 -> key with the same order; -0.0 is mapped to the key of +0.0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -46,6 +47,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   int* wsum = reinterpret_cast<int*>(hsum + 2 * kBins);  // [32]
   int* misc = wsum + 32;                             // [48]
   int* cnts = misc + 48;                             // [2]: this CTA's (#greater, #equal)
+  // per-warp lists of the keys still in the running after two passes (passes 3 and 4
+  // scan only these; a warp with more candidates than its list holds scans its keys)
+  uint32_t* clist = reinterpret_cast<uint32_t*>(cnts + 2);  // [kWarps][kListPerWarp]
 
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
@@ -126,6 +130,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   uint32_t prefix = 0u, pmask = 0u;
   int remaining = cnt;  // how many keys >= the threshold are still to be taken inside the prefix class
   const int rounds = (mine + kThreads - 1) / kThreads;
+  const int warp_id = tid >> 5;
+  uint32_t* wlist = clist + warp_id * kListPerWarp;
+  int wcnt = 0;  // candidates of this warp after two passes (warp-uniform)
+  const bool lists = rounds > 8;  // on short slices the list costs more than the scans it saves
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
@@ -133,15 +141,26 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int i = lane; i < kBins; i += 32) hw[i] = 0u;  // this warp's own histogram
     __syncwarp();
     // warp-aggregated counting, eight independent steps at a time: lanes with the
-    // same digit add once, into their warp's histogram
-    for (int rb = 0; rb < rounds; rb += 8) {
+    // same digit add once, into their warp's histogram.  Passes 1-2 scan every key
+    // of the slice; passes 3-4 only the warp's list of remaining candidates.
+    const bool from_list = lists && pass >= 2 && wcnt <= kListPerWarp;
+    const int steps = from_list ? (wcnt + 31) / 32 : rounds;
+    for (int rb = 0; rb < steps; rb += 8) {
       uint32_t dg[8];
       bool cand[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const int i = (rb + q) * kThreads + tid;
-        const bool in = i < mine;
-        const uint32_t key = in ? keys[i] : 0u;
+        bool in;
+        uint32_t key;
+        if (from_list) {
+          const int e = (rb + q) * 32 + lane;
+          in = e < wcnt;
+          key = in ? wlist[e] : 0u;
+        } else {
+          const int i = (rb + q) * kThreads + tid;
+          in = i < mine;
+          key = in ? keys[i] : 0u;
+        }
         cand[q] = in && (key & pmask) == prefix;
         dg[q] = cand[q] ? ((key >> shift) & 255u) : 0xffffffffu;
       }
@@ -166,9 +185,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     int tsum = 0;
     {
       int c = 0;
-      if (tid < kBins) {
+      if (tid < kBins) {  // the cluster's CTAs' counts of this digit, loaded together
         uint32_t* hd = &h[kBins - 1 - tid];
-        for (int rr = 0; rr < C; ++rr) c += static_cast<int>(*cluster.map_shared_rank(hd, rr));
+        uint32_t v[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) v[rr] = rr < C ? *cluster.map_shared_rank(hd, rr) : 0u;
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) c += static_cast<int>(v[rr]);
       }
       c4[0] = c;
       tsum = c;
@@ -205,6 +228,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     prefix |= static_cast<uint32_t>(digit) << shift;
     pmask |= 255u << shift;
     __syncthreads();
+    if (lists && pass == 1) {  // the keys still matching the 16-bit prefix, in this warp's list
+      const unsigned lt = (1u << lane) - 1u;
+      for (int rr = 0; rr < rounds; ++rr) {
+        const int i = rr * kThreads + tid;
+        const uint32_t key = i < mine ? keys[i] : 0u;
+        const bool c = i < mine && (key & pmask) == prefix;
+        const unsigned m = __ballot_sync(0xffffffffu, c);
+        if (c && wcnt + __popc(m & lt) < kListPerWarp) wlist[wcnt + __popc(m & lt)] = key;
+        wcnt += __popc(m);
+      }
+      __syncwarp();
+    }
   }
   const uint32_t thr = prefix;  // k-th largest key; `remaining` keys equal to it are taken
 
@@ -287,7 +322,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 }  // namespace
 
 size_t topk_smem_bytes(int per_cta) {
-  return static_cast<size_t>(per_cta) * 4 + (kWarps + 2) * kBins * 4 + (32 + 48 + 2) * 4;
+  return static_cast<size_t>(per_cta) * 4 + (kWarps + 2) * kBins * 4 + (32 + 48 + 2) * 4 +
+         static_cast<size_t>(kWarps) * kListPerWarp * 4;
 }
 
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl) {
