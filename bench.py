@@ -279,15 +279,22 @@ def run_ours(args, rank, local, world):
     torch.cuda.set_device(local)
     vbuild.build()
     w = synth.WORKLOADS[args.workload]
-    if w.layers > 1:
-        raise SystemExit("multi-layer workloads are timed by tests/test_gpu_fullsize.py, not bench.py")
+    multi = w.layers > 1
     pool = w.layer_pool(0)
     lengths = pool["prefix_len"]
-    nbytes = algorithmic_bytes(w, lengths)
+    nbytes = {k: v * w.layers for k, v in algorithmic_bytes(w, lengths).items()}
     layer_bytes = int(pool["K"].nbytes + pool["V"].nbytes)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    ncopy = max(3, -(-4 * l2 // layer_bytes) + 1)
-    states = [LayerState(w, pool, device=f"cuda:{local}") for _ in range(ncopy)]
+    if multi:
+        # every layer resident (each far larger than L2): the model's own order streams them
+        ncopy = w.layers
+        states = [LayerState(w, pool, device=f"cuda:{local}")]
+        for layer in range(1, w.layers):
+            states.append(LayerState(w, w.layer_pool(layer), device=f"cuda:{local}"))
+    else:
+        # rotating copies of the one layer, so every kernel reads its cache cold
+        ncopy = max(3, -(-4 * l2 // layer_bytes) + 1)
+        states = [LayerState(w, pool, device=f"cuda:{local}") for _ in range(ncopy)]
     stream = torch.cuda.current_stream()
     tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device=f"cuda:{local}") for s in range(w.gamma)]
 
@@ -311,20 +318,48 @@ def run_ours(args, rank, local, world):
 
     half = ncopy // 2
 
-    def step(i):  # iteration i: verify + select on copy i, the draft phase on copy i + ncopy/2
+    def step(i):
+        if multi:  # the model's order: verify every layer, select, then each draft step over the layers
+            for st in states:
+                st.verify()
+                st.select()
+            for s in range(w.gamma):
+                for st in states:
+                    st.draft_step(s, tl[s])
+            return
+        # one layer: verify + select on copy i, the draft phase on copy i + ncopy/2
         a, b = states[i % ncopy], states[(i + half) % ncopy]
         a.verify()
         a.select()
         draft_phase(b)
+
+    def phase_calls(i, which):  # the same calls as step(i), one phase only
+        if multi:
+            for st in states:
+                if which == "v":
+                    st.verify()
+                elif which == "s":
+                    st.select()
+            if which == "d":
+                for s in range(w.gamma):
+                    for st in states:
+                        st.draft_step(s, tl[s])
+            return
+        if which == "v":
+            states[i % ncopy].verify()
+        elif which == "s":
+            states[i % ncopy].select()
+        else:
+            draft_phase(states[(i + half) % ncopy])
 
     # One graph per timed run (a serving loop replays captured decode steps, so the
     # host's launch cost stays off the GPU timeline); warm-up steps in a graph of their own.
     g_warm = capture(lambda: [step(i) for i in range(args.warmup)])
     g_run = capture(lambda: [step(args.warmup + i) for i in range(args.steps)])
     # per-phase breakdown: the same calls, one phase at a time, K back to back
-    g_v = capture(lambda: [states[(args.warmup + i) % ncopy].verify() for i in range(args.steps)])
-    g_s = capture(lambda: [states[(args.warmup + i) % ncopy].select() for i in range(args.steps)])
-    g_d = capture(lambda: [draft_phase(states[(args.warmup + i + half) % ncopy]) for i in range(args.steps)])
+    g_v = capture(lambda: [phase_calls(args.warmup + i, "v") for i in range(args.steps)])
+    g_s = capture(lambda: [phase_calls(args.warmup + i, "s") for i in range(args.steps)])
+    g_d = capture(lambda: [phase_calls(args.warmup + i, "d") for i in range(args.steps)])
     torch.cuda.synchronize()
     g_warm.replay()
     torch.cuda.synchronize()
@@ -369,16 +404,16 @@ def run_ours(args, rank, local, world):
         host_in[name] = getattr(states[0], name).cpu().pin_memory()
     out_names = ("out_verify", "idx", "count", "out_draft")
     host_out = {nm: torch.empty_like(getattr(states[0], nm), device="cpu").pin_memory() for nm in out_names}
-    bi = sum(t.numel() * t.element_size() for t in host_in.values())
-    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+    bi = sum(t.numel() * t.element_size() for t in host_in.values()) * (w.layers if multi else 1)
+    bo = sum(t.numel() * t.element_size() for t in host_out.values()) * (w.layers if multi else 1)
 
     def e2e_step(i):
-        a = states[i % ncopy]
-        for nm, t in host_in.items():
-            getattr(a, nm).copy_(t, non_blocking=True)
-        a.iteration(stream=stream, select_extra=False)
-        for nm, t in host_out.items():
-            t.copy_(getattr(a, nm), non_blocking=True)
+        for a in (states if multi else [states[i % ncopy]]):  # every layer of the model, or one copy
+            for nm, t in host_in.items():
+                getattr(a, nm).copy_(t, non_blocking=True)
+            a.iteration(stream=stream, select_extra=False)
+            for nm, t in host_out.items():
+                t.copy_(getattr(a, nm), non_blocking=True)
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -395,20 +430,23 @@ def run_ours(args, rank, local, world):
     peaks = measured_peaks()
     verify_gbs = nbytes["verify"] / (t_verify * 1e-6) / 1e9
     kv_gbs = (nbytes["verify"] + nbytes["draft"]) / (ms_step * 1e-3) / 1e9
-    launches_per_step = 2 + 1 + 2 * w.gamma
+    launches_per_step = (2 + 1 + 2 * w.gamma) * (w.layers if multi else 1)
     line = {
         "metric": METRIC, "value": us_iter, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w),
-                   "l2": f"{ncopy} rotating cache copies of {layer_bytes / 1e6:.0f} MB (> 4x L2 of "
-                         f"{l2 / 1e6:.0f} MB); draft on a different copy than the verify before it",
+                   "l2": (f"{w.layers} resident layers of {layer_bytes / 1e6:.0f} MB each (L2 {l2 / 1e6:.0f} MB): "
+                          f"verify over every layer, then each draft step over every layer" if multi else
+                          f"{ncopy} rotating cache copies of {layer_bytes / 1e6:.0f} MB (> 4x L2 of "
+                          f"{l2 / 1e6:.0f} MB); draft on a different copy than the verify before it"),
                    "timing": "K steps replayed as one CUDA graph, CUDA events around it",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_bytes_per_iteration": nbytes["verify"] + nbytes["draft"],
         "kv_gbs": kv_gbs, "kv_pct_of_hbm": 100.0 * kv_gbs / peaks["hbm_gbs"],
         "phases_us": {"verify_call": t_verify, "select": t_select, "draft_gamma_steps": t_draft,
                       "per_draft_step": t_draft / max(1, w.gamma)},
+        "phases_note": "sums over the layers of one step" if multi else "one layer",
         "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine)", "bound": "hbm",
                      "achieved": verify_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": verify_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
@@ -421,10 +459,16 @@ def run_ours(args, rank, local, world):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = oracle_iteration_time(w, pool, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": statistics.mean(times) * 1e6, "unit": UNIT, "cores": cpu_threads(),
+        # sequence 0 of layer 0 is timed; the whole workload's time is scaled by prefix
+        # tokens (the verification dominates the oracle's work) and by layers
+        n0 = int(lengths[0])
+        scale = w.layers * float(sum(int(n) for n in lengths)) / n0
+        line["cpu_baseline"] = {"value": statistics.mean(times) * 1e6 * scale, "unit": UNIT, "cores": cpu_threads(),
                                 "kind": "oracle",
-                                "sample": f"{len(times)} full fp64 oracle iterations of the workload "
-                                          f"(verify, both score masks, top-k, {w.gamma} draft steps)"}
+                                "sample": f"{len(times)} fp64 oracle iterations of sequence 0 (n={n0}; verify, "
+                                          f"both score masks, top-k, {w.gamma} draft steps)"
+                                          + (f", scaled x{scale:.2f} to the workload's prefix tokens and layers"
+                                             if scale != 1.0 else ", which is the whole workload")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
