@@ -393,6 +393,30 @@ def run_ours(args, rank, local, world):
     t_verify = ph[0].elapsed_time(ph[1]) * 1e3 / args.steps
     t_select = ph[1].elapsed_time(ph[2]) * 1e3 / args.steps
     t_draft = ph[2].elapsed_time(ph[3]) * 1e3 / args.steps
+    # ---- cost of the fused logit aggregation: the verify call with no scores, with the
+    # Collect-2-Query rows and with all rows (same rotation, K back-to-back calls)
+    R = w.gamma + 1
+    variants = {"no_scores": 0, "collect2": (1 | (1 << w.gamma)), "all_rows": (1 << R) - 1}
+
+    def verify_masked(st, m0):
+        vb.vg_verify_attn(st.dims, st.cache, st.q_verify, st.k_new, st.v_new, st.prefix_len, m0, 0,
+                          st.scores0 if m0 else None, None, st.score_stride, st.out_verify, st.ws,
+                          dev_status=st.status)
+
+    score_cost = {}
+    if not multi:
+        gv = {nm: capture(lambda m0=m0: [verify_masked(states[(args.warmup + i) % ncopy], m0)
+                                         for i in range(args.steps)]) for nm, m0 in variants.items()}
+        for nm, g in gv.items():
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            ev[0].record(stream)
+            g.replay()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            score_cost[nm] = ev[0].elapsed_time(ev[1]) * 1e3 / args.steps
+        base = score_cost["no_scores"]
+        for nm in ("collect2", "all_rows"):
+            score_cost[nm + "_overhead_pct"] = 100.0 * (score_cost[nm] - base) / base
     bad = [(i, st.check_status()) for i, st in enumerate(states) if st.check_status() != 0]
     if bad:
         raise RuntimeError(f"device status (copy, code): {bad}")
@@ -447,6 +471,7 @@ def run_ours(args, rank, local, world):
         "phases_us": {"verify_call": t_verify, "select": t_select, "draft_gamma_steps": t_draft,
                       "per_draft_step": t_draft / max(1, w.gamma)},
         "phases_note": "sums over the layers of one step" if multi else "one layer",
+        "verify_call_by_score_rows_us": score_cost,
         "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine)", "bound": "hbm",
                      "achieved": verify_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": verify_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
