@@ -73,6 +73,15 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     }
     fence_mbar_init();
   }
+  // The value rows of every stage start zeroed (shared memory only, so before the
+  // dependency wait): a slot of a chunk that loads no page keeps either these zeros or
+  // a value row an earlier chunk attended, so 0 * V stays exact without zeroing rows on
+  // the producer's critical path.
+  for (int st = 0; st < kStages; ++st) {
+    uint4* vr = reinterpret_cast<uint4*>(smem + st * L.stage + L.half);
+    for (int q = threadIdx.x; q < L.half / 16; q += blockDim.x) vr[q] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();  // the zeros precede the bulk copies into the same stages
   __syncthreads();
   const int S = draft_slots(p);
   const int64_t E = static_cast<int64_t>(p.B) * S;
@@ -120,15 +129,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
           pos = ts + (jj - nsel);
         }
       }
-      if (lane < kKeys) {
-        posb[stage * kKeys + lane] = pos;
-        if (pos < 0) {  // a page not loaded this phase: zero values keep 0 * V exact
-          uint4* vr = reinterpret_cast<uint4*>(kst + L.half + lane * L.row);
-          for (int q = 0; q < page / 16; ++q) vr[q] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
+      if (lane < kKeys) posb[stage * kKeys + lane] = pos;
       const int nload = __popc(__ballot_sync(0xffffffffu, pos >= 0));
-      fence_proxy_async_smem();  // zeros written above are ordered before later bulk copies
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nload * 2 * page));
       __syncwarp();
