@@ -6,7 +6,7 @@
 // and the output lists the positions in ascending order, ready to serve as the
 // page indices of the draft's page-size-one attention (Vegas §3).
 //
-// GB300 design.  One thread-block cluster of up to 8 CTAs per sequence; each CTA
+// GB300 design.  One thread-block cluster of up to 16 CTAs per sequence; each CTA
 // keeps its contiguous slice of the scores in shared memory as order-preserving
 // 32-bit keys.  An exact MSB-first radix select (4 passes of 8 bits) finds the
 // k-th largest key: every pass builds per-warp histograms with warp-aggregated
@@ -31,6 +31,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;  // radix digit: 8 bits
 constexpr int kListPerWarp = 256;  // candidate-list capacity of a warp for the last two passes
+constexpr int kMaxCluster = 16;    // CTAs per sequence (more than 8 needs the non-portable cluster size)
 
 // fp32 -> key with the same order; -0.0 is mapped to the key of +0.0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -187,11 +188,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       int c = 0;
       if (tid < kBins) {  // the cluster's CTAs' counts of this digit, loaded together
         uint32_t* hd = &h[kBins - 1 - tid];
-        uint32_t v[8];
+        uint32_t v[kMaxCluster];
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) v[rr] = rr < C ? *cluster.map_shared_rank(hd, rr) : 0u;
+        for (int rr = 0; rr < kMaxCluster; ++rr) v[rr] = rr < C ? *cluster.map_shared_rank(hd, rr) : 0u;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) c += static_cast<int>(v[rr]);
+        for (int rr = 0; rr < kMaxCluster; ++rr) c += static_cast<int>(v[rr]);
       }
       c4[0] = c;
       tsum = c;
@@ -330,6 +331,17 @@ cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, b
   const size_t smem = topk_smem_bytes(p.per_cta);
   cudaError_t e = ensure_smem<topk_kernel>(smem);
   if (e != cudaSuccess) return e;
+  if (cluster > 8) {
+    static int nonportable[64] = {0};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!nonportable[dev]) {
+      e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable[dev] = 1;
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, p.B);
   cfg.blockDim = dim3(kThreads);

@@ -290,10 +290,10 @@ vg_status check_topk_args(const float* scores, int64_t stride, const int32_t* le
 
 vg_status run_topk(const float* scores, int64_t stride, const int32_t* len, int B, int max_len, int k, int32_t* idx,
                    int32_t* count, int32_t* dev_status, cudaStream_t stream, bool pdl) {
-  // one CTA per 4096 positions, up to a cluster of 8: the radix passes are
+  // one CTA per 4096 positions, up to a cluster of 16: the radix passes are
   // latency-bound, so shorter slices per CTA finish sooner
   int C = (max_len + 4095) / 4096;
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  C = C < 1 ? 1 : (C > 16 ? 16 : C);
   int per = (max_len + C - 1) / C;
   per = ((per + 3) / 4) * 4;
   if (per < 4) per = 4;

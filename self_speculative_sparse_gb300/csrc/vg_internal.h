@@ -14,7 +14,7 @@ namespace vg {
 constexpr int kVerifyTileKeys = 64;
 // Longest draft-token tail a sparse draft step attends besides the selection.
 constexpr int kDraftMaxTail = 64;
-// Largest sequence the top-k kernel holds in shared memory across a cluster of 8.
+// Largest sequence the top-k kernel holds (in shared memory, across a cluster of up to 16).
 constexpr int kTopkMaxLen = 262144;
 constexpr int kMaxBatch = 1024;
 
