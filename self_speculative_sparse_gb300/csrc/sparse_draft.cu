@@ -100,6 +100,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     int b = x0 / S, j = x0 - b * S;
     int stage = 0;
     uint32_t phase = 0;
+    int issued = 0;  // chunks whose copies were started
     for (int x = x0; x < x1;) {
       const int nvalid = min(kKeys, min(x1 - x, S - j));
       bool ok_wait = true;
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
         bulk_load(kst + lane * L.row, ksrc, page, &full[stage]);
         bulk_load(kst + L.half + lane * L.row, vsrc, page, &full[stage]);
       }
+      ++issued;
       x += nvalid;
       j += nvalid;
       if (j == S) {
@@ -158,6 +160,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
         phase ^= 1u;
       }
     }
+    // no copy may still be in flight when the CTA exits, also when a consumer gave up
+    // (normally the consumers have already seen every chunk land)
+    if (lane == 0)
+      for (int c = issued > kStages ? issued - kStages : 0; c < issued; ++c)
+        mbar_wait(&full[c % kStages], static_cast<uint32_t>((c / kStages) & 1), p.status);
+    __syncwarp();
     return;
   }
 

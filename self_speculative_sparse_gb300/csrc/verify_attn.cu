@@ -70,7 +70,7 @@ struct TCfg {
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin[2]
   static constexpr int NBAR = 2 * kStages + 11;
-  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag
   static constexpr int OFF_X = OFF_TMEM + 16;       // float xm[2][2][128] tile maxima, xl[128] sums
   static constexpr int OFF_META = OFF_X + 5 * 128 * 4;  // int cum[B+1], nlen[B]
   static constexpr int RWARPS = 8;                  // row warps: two per tensor-memory lane quadrant
@@ -141,8 +141,8 @@ __device__ __forceinline__ void advance(int& b, int& g, int& j, const int* cum, 
 
 
 // A wait every lane of the warp takes together (so a lost wait cannot split the warp).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, status, abort));
 }
 
 template <int D, int MR>
@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
   uint64_t* q_ready = s_full + 8;
   uint64_t* fin = s_full + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
+  // Raised by the first wait that runs out; every later wait then gives up at once.
+  // The TMA producer and the two issuers stop and drain what they started; the row
+  // warps run their loops to the end without waiting, so that the warp pairs' named
+  // barriers still match and no thread is left behind at one.
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_TMEM + 4);
   int* cum = reinterpret_cast<int*>(smem + C::OFF_META);
   int* nlen = cum + p.B + 1;
 
@@ -186,6 +191,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     mbar_init(q_ready, C::RWARPS);
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
+    *abort = 0;
     fence_mbar_init();
   }
   if (warp == C::RWARPS + 1) tc_alloc(tmem_slot, C::TMEM_COLS);  // (and frees it at the end)
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % S;
-      if (i >= S && !mbar_wait(&empty[st], ((i / S) - 1) & 1, p.status)) break;
+      if (i >= S && !mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort)) break;
       fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
       mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
       uint8_t* kdst = smem + st * C::STAGE_BYTES;
@@ -251,12 +257,12 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     int seg = 0;
     for (int i = 0; i < ntiles; ++i) {
       if (i == 0 || j == 0) {  // a new run: its query rows must be in shared memory
-        if (!mbar_wait(q_ready, seg & 1, p.status)) break;
+        if (!mbar_wait_ab(q_ready, seg & 1, p.status, abort)) break;
         ++seg;
       }
       const int st = i % S;
-      if (!mbar_wait(&full[st], (i / S) & 1, p.status)) break;
-      if (i >= 2 && !mbar_wait(&s_free[i & 1], ((i - 2) >> 1) & 1, p.status)) break;
+      if (!mbar_wait_ab(&full[st], (i / S) & 1, p.status, abort)) break;
+      if (i >= 2 && !mbar_wait_ab(&s_free[i & 1], ((i - 2) >> 1) & 1, p.status, abort)) break;
       tc_fence_after();
       const uint32_t kaddr = base + st * C::STAGE_BYTES;
 #pragma unroll
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     locate(t0, cum, p.B, p.Hkv, b, g, j);
     for (int i = 0; i < ntiles; ++i) {
       const bool first = (i == 0) || (j == 0);  // the first tile of a run overwrites O
-      if (!mbar_wait(&p_full[i & 1], (i >> 1) & 1, p.status)) break;
+      if (!mbar_wait_ab(&p_full[i & 1], (i >> 1) & 1, p.status, abort)) break;
       tc_fence_after();
       const int st = i % S;
       const uint32_t vaddr = base + st * C::STAGE_BYTES + C::TILE_BYTES;
@@ -316,9 +322,8 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     float* xl = xm + 4 * 128;                               // [row]
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
-    bool ok = true;
     int i = 0;
-    while (i < ntiles && ok) {
+    while (i < ntiles) {
       const int n_b = nlen[b];
       const int seg_first = i;
       const int seg_end = min(ntiles, i + (cum[b + 1] - cum[b] - j));
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
       float m = NEG, l = 0.f;
       for (; i < seg_end; ++i, ++j) {
         const int valid = min(TK, n_b - j * TK) - half * HK;  // keys of this half inside the prefix
-        if (!warp_wait(&s_full[i & 1], (i >> 1) & 1, p.status)) { ok = false; break; }
+        warp_wait(&s_full[i & 1], (i >> 1) & 1, p.status, abort);
         tc_fence_after();
         float s[HK];
         if (wact) tc_ld32_sync(tl + C::COL_S + (i & 1) * TK + half * HK, s);
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         if (vt_keys < TK) {
           // rows past the prefix end hold whatever the cache has there; their P is
           // zero, and zeroed V rows keep 0 * V exact even if the slots are not finite
-          if (!warp_wait(&full[i % S], (i / S) & 1, p.status)) { ok = false; break; }
+          warp_wait(&full[i % S], (i / S) & 1, p.status, abort);
           uint8_t* vt = smem + (i % S) * C::STAGE_BYTES + C::TILE_BYTES;
           for (int e = rtid; e < C::HALVES * TK * 8; e += NR) {
             const int h = e / (TK * 8), r = (e >> 3) & (TK - 1);
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
             const float alpha = resc ? ex2(m - mn) : 1.f;
             l *= alpha;
             if (half == 0) {
-              if (!warp_wait(&p_free[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status)) { ok = false; break; }
+              warp_wait(&p_free[(i - 1) & 1], ((i - 1) >> 1) & 1, p.status, abort);
               tc_fence_after();
 #pragma unroll 1
               for (int c0 = 0; c0 < D; c0 += 32) {
@@ -418,8 +423,14 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
             }
           }
           m = mn;
-          // P of this tile goes to the buffer P V of tile i - 2 read
-          if (i >= 2 && !warp_wait(&p_free[i & 1], ((i - 2) >> 1) & 1, p.status)) { ok = false; break; }
+        }
+        // P of this tile goes to the buffer P V of tile i - 2 read.  Every row warp waits,
+        // also one whose lanes hold no row in use: its arrival on p_full must not run
+        // ahead into the phase of tile i - 2 (its own S wait only bounds it by the
+        // s_free phase of that tile), or P V of tile i - 2 could start before an active
+        // warp has written its P rows.
+        if (i >= 2) warp_wait(&p_free[i & 1], ((i - 2) >> 1) & 1, p.status, abort);
+        if (wact) {
           if (is_row) {
             uint32_t pk[HK / 2];
             float ls = 0.f;
@@ -430,8 +441,11 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
                 p0 = c < valid ? p0 : 0.f;
                 p1 = c + 1 < valid ? p1 : 0.f;
               }
-              ls += p0 + p1;
+              // the sum takes the bf16 values P V multiplies, so a row's weights sum to one
+              // up to fp32 rounding (with the lazily raised max a dominant P is not a
+              // power of two, and its bf16 rounding would otherwise shift the row)
               pk[c / 2] = pack_bf16(p0, p1);
+              ls = add_bf16x2_f32(pk[c / 2], ls);
             }
             l += ls;
             uint8_t* prow = sP + (i & 1) * C::P_BYTES + row * 128;
@@ -460,7 +474,6 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[i & 1]);
       }
-      if (!ok) break;
       // run partial: (O, max, sum) of each query row once P V of its last tile landed
       const int last = i - 1;
       if (QR * quad < p.M) {  // the two halves' sums meet in the low half
@@ -468,7 +481,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         named_bar(2 + quad, 64);
       }
       if (half == 0) {
-        if (!warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status)) break;
+        warp_wait(&p_free[last & 1], (last >> 1) & 1, p.status, abort);
         tc_fence_after();
         if (QR * quad < p.M) {
           const size_t prow = (static_cast<size_t>(blockIdx.x) + static_cast<size_t>(b) * p.Hkv + g) * p.Mpad + row;

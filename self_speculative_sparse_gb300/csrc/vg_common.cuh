@@ -72,6 +72,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   }
 }
 
+// As mbar_wait, for kernels whose roles wait on one another: the first wait that runs
+// out raises the CTA's abort flag (shared memory), and every wait of the CTA then
+// gives up at once, so a broken wait costs one limit, not one per remaining wait.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        report(status, VG_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ bulk copies
 // 2-D tiled TMA load of box (x, y) into shared memory; completion is counted on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -147,6 +166,15 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+// acc + lo + hi for a packed bf16 pair, each half widened exactly to fp32 (the
+// mixed-precision add of sm_100 and later: one instruction per element).
+__device__ __forceinline__ float add_bf16x2_f32(uint32_t w, float acc) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+      : "=f"(d)
+      : "r"(w), "f"(acc));
+  return d;
 }
 // 2^x on the special-function unit (MUFU.EX2), flushing subnormal results.
 __device__ __forceinline__ float ex2(float x) {

@@ -145,3 +145,38 @@ def test_full_size_multilayer_loop_matches_oracle_on_samples():
         st.iteration()
         check_layer(w, pool, st, layer, rng, rows_v=2, rows_d=2)
         del st
+
+
+@pytest.mark.parametrize("name,layer,reps", [("loop32", 6, 40), ("batched", 0, 40)])
+def test_full_size_repeats_are_bit_identical(name, layer, reps):
+    """The same call on the same inputs gives the same bits, every time.
+
+    Every CTA of the verify kernel runs some 200+ tiles here, with warps whose lanes
+    hold no rows in use beside the ones that do: a missing wait between them shows up
+    as one lane quadrant's partial differing from run to run.  The whole iteration
+    (verify, both selections, the draft steps) is repeated as well."""
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = W[name]
+    st = LayerState(w, w.layer_pool(layer))
+    ref = None
+    for r in range(reps):
+        st.verify()
+        torch.cuda.synchronize()
+        assert st.check_status() == 0
+        cur = (st.out_verify.view(torch.int16).clone(), st.scores0.clone())
+        if ref is None:
+            ref = cur
+        else:
+            assert torch.equal(cur[0], ref[0]), f"verify output differs on repeat {r}"
+            assert torch.equal(cur[1], ref[1]), f"scores differ on repeat {r}"
+    st.iteration()
+    torch.cuda.synchronize()
+    iref = (st.out_verify.view(torch.int16).clone(), st.idx.clone(), st.out_draft.view(torch.int16).clone())
+    assert torch.equal(iref[0], ref[0])
+    for r in range(reps // 4):
+        st.iteration()
+        torch.cuda.synchronize()
+        assert st.check_status() == 0
+        assert torch.equal(st.out_verify.view(torch.int16), iref[0]), f"iteration {r}: verify output differs"
+        assert torch.equal(st.idx, iref[1]), f"iteration {r}: selection differs"
+        assert torch.equal(st.out_draft.view(torch.int16), iref[2]), f"iteration {r}: draft output differs"
