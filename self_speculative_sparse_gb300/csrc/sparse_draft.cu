@@ -280,16 +280,19 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
       pl = v.y;
     }
   }
+  // (rows past nseg, or of a CTA with no entries, read as zeros: their weight is zero
+  // and the row holds whatever was there)
   float v[kCombineRows][PER];
 #pragma unroll
   for (int q = 0; q < kCombineRows; ++q) {
     const int si = warp + kCombineWarps * q;
-    const float* src = p.part_o + prow(si < nseg ? si : 0) * D + lane * PER;  // a readable row
+    const bool ok = si < nseg && split_nonempty(cf + si, E, p.nctas);
+    const float* src = p.part_o + prow(ok ? si : 0) * D + lane * PER;
     if constexpr (PER == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(src);
+      const float4 x = ok ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
       v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
     } else {
-      const float2 x = *reinterpret_cast<const float2*>(src);
+      const float2 x = ok ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
       v[q][0] = x.x; v[q][1] = x.y;
     }
   }
@@ -320,6 +323,7 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   }
   for (int q = kCombineRows; warp + kCombineWarps * q < nseg; ++q) {  // rare: more partials per warp
     const float wq = __shfl_sync(0xffffffffu, wt, q);
+    if (!split_nonempty(cf + warp + kCombineWarps * q, E, p.nctas)) continue;  // (warp-uniform)
     const float* src = p.part_o + prow(warp + kCombineWarps * q) * D + lane * PER;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] += wq * src[e];

@@ -583,16 +583,18 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
         ls = v.y;
       }
     };
+    // (rows past nseg, or of a CTA with no items, read as zeros: their weight is zero
+    // and the row holds whatever was there)
     auto load_rows = [&](int s0, float (&v)[NB][PER]) {
 #pragma unroll
       for (int q = 0; q < NB; ++q) {
-        const int si = s0 + q < nseg ? s0 + q : 0;  // a readable row; unused if past nseg
-        const float* src = p.part_o + prow(si) * D + lane * PER;
+        const bool ok = s0 + q < nseg && split_nonempty(cf + s0 + q, T, p.nctas);
+        const float* src = p.part_o + prow(ok ? s0 + q : 0) * D + lane * PER;
         if constexpr (PER == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src);
+          const float4 x = ok ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
           v[q][0] = x.x; v[q][1] = x.y; v[q][2] = x.z; v[q][3] = x.w;
         } else {
-          const float2 x = *reinterpret_cast<const float2*>(src);
+          const float2 x = ok ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
           v[q][0] = x.x; v[q][1] = x.y;
         }
       }
@@ -708,19 +710,253 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
     if ((ms ? p.mask1 : p.mask0) == 0u || dst == nullptr) continue;
     const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.s_stride + pos;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int q = 0; q < parts; ++q) {  // rows are s_stride (a multiple of 64) apart: in bounds
-      const float4 v = *reinterpret_cast<const float4*>(src + static_cast<size_t>(q) * p.s_stride);
-      a.x += v.x;
-      a.y += v.y;
-      a.z += v.z;
-      a.w += v.w;
+    for (int q0 = 0; q0 < parts; q0 += 16) {  // one round of loads up to H_kv = 8
+      float4 v[16];  // rows are s_stride (a multiple of 64) apart: in bounds
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q0 + q < parts) v[q] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(q0 + q) * p.s_stride);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q0 + q < parts) {
+          a.x += v[q].x;
+          a.y += v[q].y;
+          a.z += v[q].z;
+          a.w += v[q].w;
+        }
     }
     float* d = dst + static_cast<size_t>(b) * p.score_stride + pos;
     d[0] = a.x;
     if (pos + 1 < n) d[1] = a.y;
     if (pos + 2 < n) d[2] = a.z;
     if (pos + 3 < n) d[3] = a.w;
+  }
+}
+
+// The same merge for a grid with few (sequence, KV head) pairs: spread over many
+// small CTAs, so that each SM moves little.  128-thread CTAs; a row's D outputs are
+// split over D/32 warps, one element per lane (RPC rows per CTA).  Everything that
+// needs only the call's inputs happens before the dependency wait: the sequence's tile
+// counts (from the lengths), the query and verify-row K/V staged in shared memory,
+// and the row's causal part (max, sum and output over its own keys u <= t).  After
+// the wait, one round of loads (up to kNarrowRound partials a lane) and a merge in a
+// fixed order: the causal part, then the partials by CTA.  Role B: CTAs of 256 prefix
+// positions, 2 per thread.
+constexpr int kNarrowThreads = 128;
+constexpr int kNarrowRound = 32;  // partial rows a lane loads in one round
+constexpr int kMaxR = 16;         // verify rows (gamma + 1 <= 16)
+
+// Tiles of one KV head before sequence b and of b, the total, and b's checked length
+// (-1 if its length or slots are out of range: the verify kernel reports that).  One
+// warp; the same checks and counts as the verify kernel's own.
+__device__ void combine_seq_meta(const VerifyParams& p, int b, int* out4) {
+  const int lane = threadIdx.x & 31;
+  int before = 0, total = 0, mine = 0, nb = -1;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int bb = b0 + lane;
+    int tiles = 0, n = -1;
+    if (bb < p.B) {
+      n = p.prefix_len[bb];
+      const int64_t off = p.seq_offset[bb];
+      if (!(n >= 0 && n <= p.max_len && off >= 0 && off + (int64_t)n + p.R <= p.capacity)) n = -1;
+      tiles = n > 0 ? (n + TK - 1) / TK : 0;
+    }
+    int tb = bb < b ? tiles : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tb += __shfl_xor_sync(0xffffffffu, tb, o);
+      tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+    }
+    before += tb;
+    total += tiles;
+    const bool here = b >= b0 && b < b0 + 32;
+    const int nsh = __shfl_sync(0xffffffffu, n, here ? b - b0 : 0);
+    if (here) {
+      nb = nsh;
+      mine = nsh > 0 ? (nsh + TK - 1) / TK : 0;
+    }
+  }
+  if (lane == 0) {
+    out4[0] = before;
+    out4[1] = mine;
+    out4[2] = total;
+    out4[3] = nb;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kNarrowThreads, 4) verify_combine_narrow_kernel(const VerifyParams p) {
+  constexpr int WPR = D / 32;                       // warps per row
+  constexpr int RPC = (kNarrowThreads / 32) / WPR;  // rows per CTA
+  constexpr int PD = D / 32;                        // elements of a dot product per lane
+  __shared__ __align__(16) __nv_bfloat16 sq[RPC][D];        // this CTA's query rows
+  __shared__ __align__(16) __nv_bfloat16 skv[2][kMaxR][D];  // the verify rows' keys and values
+  __shared__ int smeta[4];
+  pdl_launch_dependents();  // the selection kernel may start its prologue
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float NEG = neg_inf();
+  const int rblocks = (p.M + RPC - 1) / RPC;  // CTAs per (sequence, KV head)
+  const int nA = p.B * p.Hkv * rblocks;
+  if (static_cast<int>(blockIdx.x) < nA) {
+    const int bg = blockIdx.x / rblocks;
+    const int r0 = (blockIdx.x - bg * rblocks) * RPC;
+    const int g = bg % p.Hkv, b = bg / p.Hkv;
+    const int G = p.G;
+    const int rw = warp / WPR;                 // this warp's row within the CTA
+    const int r = r0 + rw;
+    const int d = (warp % WPR) * 32 + lane;    // this lane's output element
+    const bool active = r < p.M;
+    const int t = active ? r / G : 0, jh = r - t * G;
+    const int tmax = min(p.M - 1, r0 + RPC - 1) / G;  // last verify row of this CTA
+    // ---- before the dependency wait: the call's inputs only
+    if (warp == 0) combine_seq_meta(p, b, smeta);
+    __syncthreads();
+    const int n = smeta[3];
+    if (n < 0) return;  // the whole CTA
+    const int64_t base = p.seq_offset[b];
+    const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
+    const __nv_bfloat16* kn = p.k_new ? p.k_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
+                                      : p.K + ((base + n) * p.Hkv + g) * D;
+    const __nv_bfloat16* vn = p.v_new ? p.v_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
+                                      : p.V + ((base + n) * p.Hkv + g) * D;
+    constexpr int CH = D / 8;  // 16-byte chunks of a row
+    for (int e = tid; e < 2 * (tmax + 1) * CH; e += kNarrowThreads) {
+      const int which = e / ((tmax + 1) * CH), rem = e - which * (tmax + 1) * CH;
+      const int u = rem / CH, c = rem - u * CH;
+      reinterpret_cast<uint4*>(&skv[which][u][0])[c] =
+          reinterpret_cast<const uint4*>((which ? vn : kn) + u * row_stride)[c];
+    }
+    for (int e = tid; e < RPC * CH; e += kNarrowThreads) {
+      const int rr = e / CH, c = e - rr * CH;
+      const int r2 = r0 + rr;
+      if (r2 < p.M) {
+        const int t2 = r2 / G, j2 = r2 - t2 * G;
+        reinterpret_cast<uint4*>(&sq[rr][0])[c] = reinterpret_cast<const uint4*>(
+            p.q + ((static_cast<size_t>(b) * p.R + t2) * p.Hq + g * G + j2) * D)[c];
+      }
+    }
+    __syncthreads();
+    if (!active) return;
+    // causal part of this row: its own keys u = 0..t (at least itself)
+    float mc = NEG, lc = 0.f, oc = 0.f;
+    {
+      float qv[PD];
+#pragma unroll
+      for (int e = 0; e < PD; ++e) qv[e] = bf2f(sq[rw][lane * PD + e]);
+      float lg[kMaxR];
+#pragma unroll
+      for (int u = 0; u < kMaxR; ++u) {
+        lg[u] = NEG;
+        if (u <= t) {
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < PD; ++e) acc += qv[e] * bf2f(skv[0][u][lane * PD + e]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          lg[u] = acc * p.scale_log2;
+          mc = fmaxf(mc, lg[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxR; ++u) {
+        if (u <= t) {
+          const float w = ex2(lg[u] - mc);
+          lc += w;
+          oc += w * bf2f(skv[1][u][d]);
+        }
+      }
+    }
+    // ---- after the wait: the verify kernel's partials of this (sequence, KV head),
+    // written by CTAs cf..cl of its split
+    pdl_wait();
+    const int tiles = smeta[1];
+    const int64_t T = static_cast<int64_t>(p.Hkv) * smeta[2];
+    int64_t cf = 0, cl = -1;
+    if (tiles > 0) {
+      const int64_t S = static_cast<int64_t>(p.Hkv) * smeta[0] + static_cast<int64_t>(g) * tiles;
+      cf = owner_cta(S, T, p.nctas);
+      cl = owner_cta(S + tiles - 1, T, p.nctas);
+    }
+    const int nseg = static_cast<int>(cl - cf + 1);
+    const size_t pair = static_cast<size_t>(b) * p.Hkv + g;
+    float Mr = mc, lr = lc, acc = oc;  // running merge, starting with the causal part
+    for (int s0 = 0; s0 < nseg; s0 += kNarrowRound) {
+      const int ns = min(kNarrowRound, nseg - s0);
+      float mv = NEG, lv = 0.f;
+      if (lane < ns && split_nonempty(cf + s0 + lane, T, p.nctas)) {  // CTAs with no items wrote none
+        const float2 v = *reinterpret_cast<const float2*>(
+            p.part_ml + ((static_cast<size_t>(cf + s0 + lane) + pair) * p.Mpad + r) * 2);
+        mv = v.x;
+        lv = v.y;
+      }
+      float ov[kNarrowRound];  // (0 for a CTA with no items: its row holds whatever was there)
+#pragma unroll
+      for (int q = 0; q < kNarrowRound; ++q)
+        ov[q] = q < ns && split_nonempty(cf + s0 + q, T, p.nctas)
+                    ? p.part_o[((static_cast<size_t>(cf + s0 + q) + pair) * p.Mpad + r) * D + d]
+                    : 0.f;
+      float mx = mv;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float Mn = fmaxf(Mr, mx);
+      const float sc = ex2(Mr - Mn);  // Mr is finite: the causal part has at least one key
+      acc *= sc;
+      lr *= sc;
+      Mr = Mn;
+      const float w = mv != NEG ? ex2(mv - Mr) : 0.f;
+      float wl = w * lv;  // fixed-order butterfly
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, off);
+      lr += wl;
+#pragma unroll
+      for (int q = 0; q < kNarrowRound; ++q) {
+        const float wq = __shfl_sync(0xffffffffu, w, q);
+        if (q < ns) acc += wq * ov[q];
+      }
+    }
+    p.out[((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + d] = __float2bfloat16_rn(acc / lr);
+    if (p.k_new && jh == 0) {  // append verify row t (the chain enters the cache)
+      const size_t dst = ((base + n + t) * p.Hkv + g) * D + d;
+      p.K[dst] = skv[0][t][d];
+      p.V[dst] = skv[1][t][d];
+    }
+    return;
+  }
+  // score role: fixed-order sum of the per-(KV head, part) partial scores, 2 positions a
+  // thread, each mask's parts loaded in one round (up to H_kv = 8)
+  constexpr int CHS = kNarrowThreads * 2;
+  const int nchunks = (p.max_len + CHS - 1) / CHS;
+  const int sb = blockIdx.x - nA;
+  const int b = sb / nchunks, ch = sb - b * nchunks;
+  if (b >= p.B) return;
+  const int n = p.prefix_len[b];
+  {
+    const int64_t off = p.seq_offset[b];
+    if (!(n >= 0 && n <= p.max_len && off >= 0 && off + (int64_t)n + p.R <= p.capacity)) return;
+  }
+  const int pos = ch * CHS + tid * 2;
+  if (pos >= n) return;
+  pdl_wait();
+  const int parts = p.Hkv * 2;
+  for (int ms = 0; ms < 2; ++ms) {
+    float* dst = ms ? p.scores1 : p.scores0;
+    if ((ms ? p.mask1 : p.mask0) == 0u || dst == nullptr) continue;
+    const float* src = p.part_s + (static_cast<size_t>(ms) * p.B + b) * parts * p.s_stride + pos;
+    float2 a = make_float2(0.f, 0.f);
+    for (int q0 = 0; q0 < parts; q0 += 16) {
+      float2 v[16];  // rows are s_stride (a multiple of 64) apart: in bounds
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q0 + q < parts) v[q] = *reinterpret_cast<const float2*>(src + static_cast<size_t>(q0 + q) * p.s_stride);
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q0 + q < parts) {
+          a.x += v[q].x;
+          a.y += v[q].y;
+        }
+    }
+    float* dd = dst + static_cast<size_t>(b) * p.score_stride + pos;
+    dd[0] = a.x;
+    if (pos + 1 < n) dd[1] = a.y;
   }
 }
 
@@ -744,12 +980,7 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
     }
     return e;
   }
-  const int nA = p.B * p.Hkv * ((p.M + kCombineWarps - 1) / kCombineWarps);
-  constexpr int CH = kCombineWarps * 32 * 4;
-  const int nS = ((p.mask0 | p.mask1) != 0u) ? p.B * ((p.max_len + CH - 1) / CH) : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nA + nS);
-  cfg.blockDim = dim3(kCombineWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
@@ -757,6 +988,22 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  const bool scores = (p.mask0 | p.mask1) != 0u;
+  // few (sequence, KV head) pairs: the narrow combine spreads the merge over many SMs
+  constexpr int RPCN = (kNarrowThreads / 32) / (D / 32);
+  const int nAn = p.B * p.Hkv * ((p.M + RPCN - 1) / RPCN);
+  if (nAn <= 2 * p.nctas) {
+    constexpr int CHS = kNarrowThreads * 2;
+    const int nSn = scores ? p.B * ((p.max_len + CHS - 1) / CHS) : 0;
+    cfg.gridDim = dim3(nAn + nSn);
+    cfg.blockDim = dim3(kNarrowThreads);
+    return cudaLaunchKernelEx(&cfg, verify_combine_narrow_kernel<D>, p);
+  }
+  const int nA = p.B * p.Hkv * ((p.M + kCombineWarps - 1) / kCombineWarps);
+  constexpr int CH = kCombineWarps * 32 * 4;
+  const int nS = scores ? p.B * ((p.max_len + CH - 1) / CH) : 0;
+  cfg.gridDim = dim3(nA + nS);
+  cfg.blockDim = dim3(kCombineWarps * 32);
   return cudaLaunchKernelEx(&cfg, verify_combine_kernel<D>, p);
 }
 

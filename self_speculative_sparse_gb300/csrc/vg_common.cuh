@@ -296,9 +296,13 @@ __host__ __device__ __forceinline__ int64_t owner_cta(int64_t x, int64_t T, int6
   return ((x + 1) * N - 1) / T;
 }
 __host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t T, int64_t N) { return (c * T) / N; }
-// True if CTA c of that split owns at least one item (with T < N some own none).
+// True if CTA c (0 <= c < N) of that split owns at least one item.  Every CTA does when
+// T >= N; otherwise (c + 1) * T < N * N, so 32-bit arithmetic is exact (and cheap:
+// a 64-bit division is a long instruction sequence, and callers test many CTAs).
 __host__ __device__ __forceinline__ bool split_nonempty(int64_t c, int64_t T, int64_t N) {
-  return split_begin(c, T, N) < split_begin(c + 1, T, N);
+  if (T >= N) return true;
+  const int ci = static_cast<int>(c), ti = static_cast<int>(T), ni = static_cast<int>(N);
+  return (ci * ti) / ni < ((ci + 1) * ti) / ni;
 }
 
 // Sets a kernel's dynamic shared-memory limit once per device (and again only if a

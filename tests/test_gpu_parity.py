@@ -42,13 +42,17 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("fill", [0x7F, 0xFF], ids=["ws_huge", "ws_nan"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_iteration_matches_oracle(name):
+def test_iteration_matches_oracle(name, fill):
     from self_speculative_sparse_gb300.runtime import LayerState
     w = CASES[name]
     pool = w.layer_pool(0)
     st = LayerState(w, pool)
-    st.ws.fill_(0x7F)             # garbage workspace: results must not depend on its contents
+    # garbage workspace: results must not depend on its contents, finite (0x7F: 3.4e38)
+    # or not (0xFF: NaN), also where a split leaves CTAs without work between the
+    # ones that hold a (sequence, KV head)
+    st.ws.fill_(fill)
     st.iteration()
     torch.cuda.synchronize()
     assert st.check_status() == 0, f"device status {st.check_status()}"
