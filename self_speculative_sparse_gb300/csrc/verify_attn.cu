@@ -68,8 +68,8 @@ struct TCfg {
   static constexpr int OFF_Q = kStages * STAGE_BYTES;
   static constexpr int OFF_P = OFF_Q + HALVES * QHALF;  // two P buffers
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin[2]
-  static constexpr int NBAR = 2 * kStages + 11;
+  // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin[2], q_landed
+  static constexpr int NBAR = 2 * kStages + 12;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag
   static constexpr int OFF_X = OFF_TMEM + 16;       // float xm[2][2][128] tile maxima, xl[128] sums
   static constexpr int OFF_META = OFF_X + 5 * 128 * 4;  // int cum[B+1], nlen[B]
@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
   uint64_t* p_free = s_full + 6;
   uint64_t* q_ready = s_full + 8;
   uint64_t* fin = s_full + 9;
+  uint64_t* q_landed = s_full + 11;  // the first run's query rows are in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
   // Raised by the first wait that runs out; every later wait then gives up at once.
   // The TMA producer and the two issuers stop and drain what they started; the row
@@ -176,7 +177,9 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
   const int nsc = 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));  // score rows
   const int arows = p.M + nsc;                                   // A-operand rows in use
 
-  if (warp == 0) seq_meta(p, cum, nlen);
+  // Launched as a programmatic dependent: shared and tensor memory are set up while
+  // the previous kernel in the stream finishes; nothing in global memory (the
+  // lengths, the inputs, the cache, the workspace) is read or written before the wait.
   if (threadIdx.x == 32) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     mbar_init(q_ready, C::RWARPS);
     mbar_init(&fin[0], 1);
     mbar_init(&fin[1], 1);
+    mbar_init(q_landed, C::RWARPS);
     *abort = 0;
     fence_mbar_init();
   }
@@ -210,6 +214,8 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     }
   }
   fence_proxy_async_smem();
+  pdl_wait();
+  if (warp == 0) seq_meta(p, cum, nlen);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -232,6 +238,9 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % S;
+      // after the first stage, the first run's query rows go first: issued together
+      // with the whole ring, their loads would queue behind it (about 3 us at the start)
+      if (i == 1 && !mbar_wait_ab(q_landed, 0, p.status, abort)) break;
       if (i >= S && !mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort)) break;
       fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
       mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
@@ -336,6 +345,10 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         *reinterpret_cast<uint4*>(sQ + (c >> 3) * C::QHALF + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
       }
       named_bar(1, NR);
+      if (seg_first == 0) {  // (the TMA producer holds back the ring until then)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_landed);
+      }
       // score rows: column d of each mask's summed query, split into bf16 high + low
       if (nsc > 0 && rtid < D) {
         const int cc = rtid & 63;
@@ -344,10 +357,11 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
           const uint32_t mk = ms ? p.mask1 : p.mask0;
           if (mk == 0u) continue;
           float acc = 0.f;
-          for (int r = 0; r < p.M; ++r) {
-            if (((mk >> (r / p.G)) & 1u) == 0u) continue;
-            acc += bf2f(*reinterpret_cast<const __nv_bfloat16*>(sQ + (rtid >> 6) * C::QHALF + r * 128 +
-                                                                 (((cc >> 3) ^ (r & 7)) << 4) + (cc & 7) * 2));
+          for (uint32_t bits = mk; bits != 0u; bits &= bits - 1u) {  // the mask's rows t, then heads
+            const int r0 = (__ffs(bits) - 1) * p.G;
+            for (int r = r0; r < r0 + p.G; ++r)
+              acc += bf2f(*reinterpret_cast<const __nv_bfloat16*>(sQ + (rtid >> 6) * C::QHALF + r * 128 +
+                                                                   (((cc >> 3) ^ (r & 7)) << 4) + (cc & 7) * 2));
           }
           const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
           const __nv_bfloat16 lo = __float2bfloat16_rn(acc - bf2f(hi));
@@ -967,8 +981,19 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
   const size_t smem = C::smem(p.B);
   cudaError_t e = ensure_smem<verify_kernel<D, MR>>(smem);
   if (e != cudaSuccess) return e;
-  verify_kernel<D, MR><<<p.nctas, C::THREADS, smem, stream>>>(p, tmK, tmV);
-  e = cudaGetLastError();
+  {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nctas);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, verify_kernel<D, MR>, p, tmK, tmV);
+  }
   if (e != cudaSuccess) {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, verify_kernel<D, MR>) == cudaSuccess) {

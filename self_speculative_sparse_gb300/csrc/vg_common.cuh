@@ -291,11 +291,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // CTA of a balanced contiguous split of T items over N CTAs that owns item x:
-// CTA c owns [floor(c T / N), floor((c+1) T / N)).
+// CTA c owns [floor(c T / N), floor((c+1) T / N)).  (A 64-bit division is a long
+// instruction sequence on the GPU: when the products fit in 32 bits, as they do for
+// T < 2^22 items over at most 512 CTAs, the division is done in 32 bits.)
 __host__ __device__ __forceinline__ int64_t owner_cta(int64_t x, int64_t T, int64_t N) {
+  if (T < (int64_t{1} << 22) && N <= 512)
+    return static_cast<int64_t>((static_cast<uint32_t>(x + 1) * static_cast<uint32_t>(N) - 1u) / static_cast<uint32_t>(T));
   return ((x + 1) * N - 1) / T;
 }
-__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t T, int64_t N) { return (c * T) / N; }
+__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t T, int64_t N) {
+  if (T < (int64_t{1} << 22) && N <= 512 && c <= N)
+    return static_cast<int64_t>(static_cast<uint32_t>(c) * static_cast<uint32_t>(T) / static_cast<uint32_t>(N));
+  return (c * T) / N;
+}
 // True if CTA c (0 <= c < N) of that split owns at least one item.  Every CTA does when
 // T >= N; otherwise (c + 1) * T < N * N, so 32-bit arithmetic is exact (and cheap:
 // a 64-bit division is a long instruction sequence, and callers test many CTAs).
