@@ -11,11 +11,13 @@
 // 32-bit keys.  An exact MSB-first radix select (4 passes of 8 bits) finds the
 // k-th largest key: every pass builds per-warp histograms with warp-aggregated
 // increments (one atomic per distinct digit per warp step, eight steps in flight,
-// no contention between warps), the cluster sums them through distributed shared
-// memory, and a block-wide scan over the digits lets every CTA pick the same
-// digit.  A final
-// cluster-wide exclusive scan in position order writes the selected positions,
-// taking the needed number of threshold-equal keys from the lowest positions.
+// no contention between warps); each CTA pushes its histogram into every CTA of the
+// cluster through distributed shared memory (stores before the cluster barrier, so
+// that after it every CTA sums the cluster's counts from its own shared memory with
+// no remote round trip), and a block-wide scan over the digits lets every CTA pick
+// the same digit.  A final cluster-wide exclusive scan in position order (the CTAs'
+// counts pushed the same way) writes the selected positions, taking the needed
+// number of threshold-equal keys from the lowest positions.
 // Everything is integer work: the result is bit-exact and deterministic.
 #include <cooperative_groups.h>
 
@@ -44,13 +46,15 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ uint32_t tk_smem[];
   uint32_t* keys = tk_smem;                          // [per_cta]
   uint32_t* hist = keys + p.per_cta;                 // [kWarps][kBins] per-warp digit histograms
-  uint32_t* hsum = hist + kWarps * kBins;            // [2][kBins] CTA histograms (double-buffered)
-  int* wsum = reinterpret_cast<int*>(hsum + 2 * kBins);  // [32]
+  // [2][kMaxCluster][kBins]: every CTA of the cluster pushes its histogram of a pass into
+  // slot (pass parity, its rank) of every CTA, so the sums are read locally
+  uint32_t* hall = hist + kWarps * kBins;
+  int* call = reinterpret_cast<int*>(hall + 2 * kMaxCluster * kBins);  // [kMaxCluster][2] (#greater, #equal), pushed
+  int* wsum = call + 2 * kMaxCluster;                // [32]
   int* misc = wsum + 32;                             // [48]
-  int* cnts = misc + 48;                             // [2]: this CTA's (#greater, #equal)
   // per-warp lists of the keys still in the running after two passes (passes 3 and 4
   // scan only these; a warp with more candidates than its list holds scans its keys)
-  uint32_t* clist = reinterpret_cast<uint32_t*>(cnts + 2);  // [kWarps][kListPerWarp]
+  uint32_t* clist = reinterpret_cast<uint32_t*>(misc + 48);  // [kWarps][kListPerWarp]
 
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
@@ -82,6 +86,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int i = tid; i < mine; i += kThreads) out[start + i] = start + i;
     return;
   }
+  // every CTA of the cluster must be running before the first push into its shared
+  // memory: arrive now, wait once the keys are loaded (the returns above are taken by
+  // the whole cluster, which shares the sequence)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   {
     // batched loads: up to 8 independent loads in flight per thread per round
     // (start is a multiple of 4 unless this is the ragged last CTA: then scalar)
@@ -126,6 +134,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   }
 
   __syncthreads();  // the passes read keys that other threads stored
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
   // ---------------------------------------------------------------- radix select
   uint32_t prefix = 0u, pmask = 0u;
@@ -173,26 +182,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
         if (cand[q] && lane == __ffs(peers[q]) - 1) atomicAdd(&hw[dg[q]], static_cast<uint32_t>(__popc(peers[q])));
     }
     __syncthreads();
-    uint32_t* h = hsum + (pass & 1) * kBins;
-    if (tid < kBins) {
+    uint32_t* hb = hall + (pass & 1) * kMaxCluster * kBins;  // [source rank][digit]
+    if (tid < kBins) {  // this CTA's count of digit tid, pushed to every CTA of the cluster
       uint32_t sum = 0;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) sum += hist[w * kBins + tid];
-      h[tid] = sum;
+      for (int rr = 0; rr < C; ++rr) *cluster.map_shared_rank(hb + r * kBins + tid, rr) = sum;
     }
-    cluster.sync();
+    cluster.sync();  // the pushes have landed (a buffer is reused two passes on, after
+                     // the next pass's sync, so no CTA still reads it)
     // cluster-wide counts, highest digit first: thread t (< 256) owns digit 255 - t
     int c4[1];
     int tsum = 0;
     {
       int c = 0;
-      if (tid < kBins) {  // the cluster's CTAs' counts of this digit, loaded together
-        uint32_t* hd = &h[kBins - 1 - tid];
-        uint32_t v[kMaxCluster];
+      if (tid < kBins) {
 #pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr) v[rr] = rr < C ? *cluster.map_shared_rank(hd, rr) : 0u;
-#pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr) c += static_cast<int>(v[rr]);
+        for (int rr = 0; rr < kMaxCluster; ++rr)
+          if (rr < C) c += static_cast<int>(hb[rr * kBins + (kBins - 1 - tid)]);
       }
       c4[0] = c;
       tsum = c;
@@ -284,22 +291,23 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       misc[8 + lane] = gi - g;   // greater keys before warp `lane`'s run
       misc[24 + lane] = ei - e;  // equal keys before it
     }
-    if (lane == kWarps - 1) {
-      cnts[0] = gi;
-      cnts[1] = ei;
+    if (lane == kWarps - 1) {  // this CTA's totals, pushed to every CTA of the cluster
+      for (int rr = 0; rr < C; ++rr) {
+        int* dst = cluster.map_shared_rank(call + 2 * r, rr);
+        dst[0] = gi;
+        dst[1] = ei;
+      }
     }
   }
-  cluster.sync();
+  cluster.sync();  // (the last access to another CTA's shared memory precedes it)
   int off = 0, eq_prev = 0, take_mine = 0;
   for (int rr = 0; rr < C; ++rr) {
-    const int g_r = *cluster.map_shared_rank(&cnts[0], rr);
-    const int e_r = *cluster.map_shared_rank(&cnts[1], rr);
+    const int g_r = call[2 * rr], e_r = call[2 * rr + 1];
     const int take_r = max(0, min(e_r, remaining - eq_prev));
     if (rr < r) off += g_r + take_r;
     if (rr == r) take_mine = take_r;
     eq_prev += e_r;
   }
-  cluster.sync();  // no CTA leaves while its counters may still be read
   const int gt_before = misc[8 + warp], eq_before = misc[24 + warp];
   int sel_base = off + gt_before + min(eq_before, take_mine);
   int eq_rank = eq_before;
@@ -323,8 +331,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 }  // namespace
 
 size_t topk_smem_bytes(int per_cta) {
-  return static_cast<size_t>(per_cta) * 4 + (kWarps + 2) * kBins * 4 + (32 + 48 + 2) * 4 +
-         static_cast<size_t>(kWarps) * kListPerWarp * 4;
+  return static_cast<size_t>(per_cta) * 4 + static_cast<size_t>(kWarps + 2 * kMaxCluster) * kBins * 4 +
+         (2 * kMaxCluster + 32 + 48) * 4 + static_cast<size_t>(kWarps) * kListPerWarp * 4;
 }
 
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl) {
