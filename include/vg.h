@@ -227,6 +227,18 @@ const char* vg_last_error(void);
 /* Library version, as major * 10000 + minor * 100 + patch. */
 int32_t vg_version(void);
 
+/* Self-test of the device-side failure path (no part of the method): launches one
+ * CTA of two warps on `stream`; each waits on an mbarrier that nothing arrives on.
+ * The first wait gives up after limit_us microseconds (1 .. 1000000), writes
+ * VG_ERR_DEVICE_TIMEOUT into *dev_status (if it holds 0) and raises the CTA's abort
+ * flag, on which the second wait (whose own limit is the library's 2 s) gives up at
+ * once.  *elapsed_ns (device memory, may be NULL) receives the time from the start
+ * of the waits to the end of both, so a caller can check that neither a lost wait
+ * nor its abort leaves a kernel running.  No copy or tensor-core operation is
+ * involved.  Returns VG_ERR_INVALID_ARG for a limit out of range or a NULL or
+ * misaligned dev_status / elapsed_ns, VG_ERR_CUDA if the launch fails. */
+vg_status vg_selftest_lost_wait(uint32_t limit_us, int32_t* dev_status, uint64_t* elapsed_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

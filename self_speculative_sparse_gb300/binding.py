@@ -23,7 +23,8 @@ VG_ERR_DEVICE_TIMEOUT = -5
 VG_ERR_DEVICE_BOUNDS = -6
 
 ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_sparse_draft_attn", "vg_iteration",
-                "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_last_error", "vg_version")
+                "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_last_error", "vg_version",
+                "vg_selftest_lost_wait")
 
 
 class VgError(RuntimeError):
@@ -88,6 +89,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_last_error.restype = ctypes.c_char_p
     L.vg_version.argtypes = []
     L.vg_version.restype = i32
+    L.vg_selftest_lost_wait.argtypes = [u32, vp, vp, vp]
+    L.vg_selftest_lost_wait.restype = i32
     if path is None:
         _lib = L
     return L
@@ -167,3 +170,8 @@ def vg_sparse_draft_attn_noalloc(dims, cache, q, k_new, v_new, idx, count, k_str
     _check(load().vg_sparse_draft_attn_noalloc(ctypes.byref(dims), ctypes.byref(cache), ptr(q), ptr(k_new),
                                                ptr(v_new), ptr(idx), ptr(count), k_stride, ptr(tail_start),
                                                ptr(tail_len), ptr(out), ptr(dev_status), _stream(stream)))
+
+
+def vg_selftest_lost_wait(limit_us, dev_status, elapsed_ns=None, stream=None) -> None:
+    """Self-test of the bounded waits: a wait that nothing completes gives up after limit_us."""
+    _check(load().vg_selftest_lost_wait(limit_us, ptr(dev_status), ptr(elapsed_ns), _stream(stream)))

@@ -12,6 +12,7 @@
 #include <string>
 
 #include "vg.h"
+#include "vg_common.cuh"
 #include "vg_internal.h"
 
 namespace vg {
@@ -370,6 +371,34 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   return VG_OK;
 }
 
+// Self-test of the bounded waits (vg_selftest_lost_wait): warp 0 waits, with a limit
+// of limit_ns, on an mbarrier that nothing arrives on; warp 1 waits on another with the
+// full limit.  The first wait runs out, reports VG_ERR_DEVICE_TIMEOUT and raises the
+// CTA's abort flag; the second must then give up at once.  No copy or MMA is tracked
+// by either mbarrier, so nothing is in flight when the CTA exits.
+__global__ void __launch_bounds__(64) lost_wait_kernel(int32_t* status, unsigned long long limit_ns,
+                                                       unsigned long long* elapsed_ns) {
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const unsigned long long t0 = globaltimer();
+  if ((threadIdx.x & 31) == 0) {
+    volatile int* ab = &abort_flag;
+    if (threadIdx.x == 0)
+      mbar_wait_ab(&bars[0], 0, status, ab, limit_ns);
+    else
+      mbar_wait_ab(&bars[1], 0, status, ab);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && elapsed_ns) *elapsed_ns = globaltimer() - t0;
+}
+
 }  // namespace
 }  // namespace vg
 
@@ -378,6 +407,19 @@ using namespace vg;
 extern "C" {
 
 int32_t vg_version(void) { return 100; }
+
+vg_status vg_selftest_lost_wait(uint32_t limit_us, int32_t* dev_status, uint64_t* elapsed_ns, void* stream) {
+  g_err.clear();
+  if (limit_us < 1 || limit_us > 1000000) return fail(VG_ERR_INVALID_ARG, "limit_us=%u outside [1, 1000000]", limit_us);
+  if (!dev_status) return fail(VG_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0 || (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u) != 0)
+    return fail(VG_ERR_INVALID_ARG, "dev_status must be 4-byte and elapsed_ns 8-byte aligned");
+  lost_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev_status, static_cast<unsigned long long>(limit_us) * 1000ull, reinterpret_cast<unsigned long long*>(elapsed_ns));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return VG_OK;
+}
 
 const char* vg_last_error(void) { return g_err.c_str(); }
 

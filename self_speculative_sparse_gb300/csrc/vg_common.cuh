@@ -75,14 +75,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
 // As mbar_wait, for kernels whose roles wait on one another: the first wait that runs
 // out raises the CTA's abort flag (shared memory), and every wait of the CTA then
 // gives up at once, so a broken wait costs one limit, not one per remaining wait.
-__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         report(status, VG_ERR_DEVICE_TIMEOUT);
         return false;

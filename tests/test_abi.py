@@ -154,3 +154,12 @@ def test_iteration_rejects_bad_arguments(lib):
 def test_workspace_size_rejects_bad_dims(lib):
     assert lib.vg_workspace_size(ctypes.byref(dims(d=80)), 16) == 0
     assert lib.vg_workspace_size(ctypes.byref(dims()), 0) == 0
+
+
+def test_lost_wait_self_test_validates_its_arguments_on_the_host(lib):
+    # checked before any CUDA call, so this runs without a device
+    for limit in (0, 1000001):
+        assert lib.vg_selftest_lost_wait(limit, Buf().addr, None, None) == vb.VG_ERR_INVALID_ARG
+    assert lib.vg_selftest_lost_wait(1000, None, None, None) == vb.VG_ERR_INVALID_ARG
+    assert lib.vg_selftest_lost_wait(1000, Buf().addr + 2, None, None) == vb.VG_ERR_INVALID_ARG
+    assert lib.vg_selftest_lost_wait(1000, Buf().addr, Buf().addr + 4, None) == vb.VG_ERR_INVALID_ARG

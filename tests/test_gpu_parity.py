@@ -207,3 +207,26 @@ def test_graph_replay_rotation_keeps_status_clean():
     torch.cuda.synchronize()
     assert [st.check_status() for st in states] == [0] * ncopy
     check_iteration(w, pool, states[0], w.rows(w.select_rows), None)
+
+
+def test_a_lost_wait_reports_a_timeout_and_the_gpu_stays_usable():
+    """The failure path of the bounded waits, made to run out on purpose (no fault, no
+    hang): a wait that nothing completes gives up after its limit and reports
+    VG_ERR_DEVICE_TIMEOUT; the CTA's abort flag makes the other wait give up at once
+    (not after its own 2 s); the next call works as usual."""
+    from self_speculative_sparse_gb300 import binding as vb
+    from self_speculative_sparse_gb300.runtime import LayerState
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(1, dtype=torch.int64, device="cuda")
+    vb.vg_selftest_lost_wait(20000, status, elapsed)
+    torch.cuda.synchronize()
+    assert int(status.item()) == vb.VG_ERR_DEVICE_TIMEOUT
+    ns = int(elapsed.item())
+    assert 20e6 <= ns < 500e6, ns
+    w = CASES["tiny"]
+    pool = w.layer_pool(0)
+    st = LayerState(w, pool)
+    st.iteration()
+    torch.cuda.synchronize()
+    assert st.check_status() == 0
+    check_iteration(w, pool, st, w.rows(w.select_rows), w.rows(w.extra_rows) if w.extra_rows else None)
