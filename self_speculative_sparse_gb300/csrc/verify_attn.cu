@@ -49,16 +49,23 @@ constexpr int TK = kVerifyTileKeys;
 // A row's running max is raised only when a tile's max exceeds it by more than this
 // (log2 units), so P stays below 2^8 and rescaling O is rare.
 constexpr float kRescaleSlack = 8.f;
+// Runs of a sequence with at most this many prefix keys carry P as a bf16 high part
+// plus a bf16 low part (P - bf16(P)), so their weights are exact to about 2^-17.  With
+// round-to-nearest the output's error from rounding P to bf16 alone is about
+// 2^-9 * sqrt(sum_i w_i^2 v_i^2), which only rows whose weight sits on a few keys bring
+// near the 2e-3 asked of the outputs; few keys make that likely.  A second P V product
+// adds the low part in; longer runs, whose weights spread, go without it.
+constexpr int kLowRunKeys = 1024;
 
 // MR: rows of the MMA (64 when the query and score rows fit, else 128).  With
 // M = 64 the accumulator's row r sits in lane 16 (r / 16) + r % 16 of quadrant r / 16.
 template <int D, int MR>
 struct TCfg {
   static constexpr int STAGE_BYTES_ = 2 * kVerifyTileKeys * D * 2;
-  static constexpr int kStages =  // as many stages as 192 KB leave beside Q and two P buffers
-      (196608 - (D / 64) * MR * 128 - 2 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_ > 12
+  static constexpr int kStages =  // as many stages as 208 KB leave beside Q and four P buffers
+      (212992 - (D / 64) * MR * 128 - 4 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_ > 12
           ? 12
-          : (196608 - (D / 64) * MR * 128 - 2 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_;
+          : (212992 - (D / 64) * MR * 128 - 4 * MR * kVerifyTileKeys * 2) / STAGE_BYTES_;
   static constexpr int HALVES = D / 64;             // 64-column (128-byte) swizzled boxes
   static constexpr int HALF_BYTES = TK * 128;       // one box of a K or V tile
   static constexpr int TILE_BYTES = TK * D * 2;
@@ -66,8 +73,8 @@ struct TCfg {
   static constexpr int QHALF = MR * 128;            // A operand: MR rows x 64 columns
   static constexpr int P_BYTES = MR * TK * 2;       // P: MR rows x 64 keys (one box wide)
   static constexpr int OFF_Q = kStages * STAGE_BYTES;
-  static constexpr int OFF_P = OFF_Q + HALVES * QHALF;  // two P buffers
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_P = OFF_Q + HALVES * QHALF;  // P high part [2], then low part [2]
+  static constexpr int OFF_BAR = OFF_P + 4 * P_BYTES;
   // full[S], empty[S], s_full[2], s_free[2], p_full[2], p_free[2], q_ready, fin[2], q_landed
   static constexpr int NBAR = 2 * kStages + 12;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag
@@ -77,8 +84,12 @@ struct TCfg {
   static constexpr int THREADS = (RWARPS + 3) * 32; // + TMA producer, Q K^T issuer, P V issuer
   static constexpr uint32_t TMEM_COLS = 256;        // O at columns [0, D), S buffers at 128 and 192
   static constexpr uint32_t COL_S = 128;
-  static size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
+  static constexpr size_t smem(int B) { return 1024 + OFF_META + (size_t)(2 * B + 1) * 4; }
 };
+// every configuration fits the 227 KB a CTA may hold at the largest batch
+static_assert(TCfg<64, 64>::smem(kMaxBatch) <= 232448 && TCfg<64, 128>::smem(kMaxBatch) <= 232448 &&
+                  TCfg<128, 64>::smem(kMaxBatch) <= 232448 && TCfg<128, 128>::smem(kMaxBatch) <= 232448,
+              "verify shared memory exceeds the per-CTA limit");
 
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
@@ -212,6 +223,8 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
       const int buf = e / pz, r = p.M + (e - buf * pz) / 8, c = e & 7;
       *reinterpret_cast<uint4*>(sP + buf * C::P_BYTES + r * 128 + c * 16) = z;
     }
+    for (int e = threadIdx.x; e < 2 * C::P_BYTES / 16; e += C::THREADS)  // (low-part rows >= M stay zero)
+      reinterpret_cast<uint4*>(sP + 2 * C::P_BYTES)[e] = z;
   }
   fence_proxy_async_smem();
   pdl_wait();
@@ -293,6 +306,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     const uint32_t base = smem_u32(smem), paddr = smem_u32(sP);
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
+    bool lo = nlen[b] <= kLowRunKeys;  // a short run: its P's low part too
     for (int i = 0; i < ntiles; ++i) {
       const bool first = (i == 0) || (j == 0);  // the first tile of a run overwrites O
       if (!mbar_wait_ab(&p_full[i & 1], (i >> 1) & 1, p.status, abort)) break;
@@ -303,9 +317,16 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
       for (int kk = 0; kk < TK / 16; ++kk)
         tc_mma(tm, tc_desc_sw128(paddr + (i & 1) * C::P_BYTES + kk * 32, 16, 1024),
                tc_desc_sw128(vaddr + kk * 2048, C::HALF_BYTES, 1024), idO, (kk > 0 || !first) ? 1u : 0u);
+      if (lo) {
+#pragma unroll
+        for (int kk = 0; kk < TK / 16; ++kk)
+          tc_mma(tm, tc_desc_sw128(paddr + (2 + (i & 1)) * C::P_BYTES + kk * 32, 16, 1024),
+                 tc_desc_sw128(vaddr + kk * 2048, C::HALF_BYTES, 1024), idO, 1u);
+      }
       tc_commit(&empty[st]);
       tc_commit(&p_free[i & 1]);
       advance(b, g, j, cum, p.B, p.Hkv);
+      if (j == 0) lo = b < p.B && nlen[b] <= kLowRunKeys;
     }
     tc_commit(&fin[1]);
     mbar_wait(&fin[1], 0, p.status);
@@ -334,6 +355,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     int i = 0;
     while (i < ntiles) {
       const int n_b = nlen[b];
+      const bool lo_run = n_b <= kLowRunKeys;  // (uniform over the CTA)
       const int seg_first = i;
       const int seg_end = min(ntiles, i + (cum[b + 1] - cum[b] - j));
       // query rows of this (sequence, KV head): row r -> (t = r / G, head g*G + r % G)
@@ -446,27 +468,51 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         if (i >= 2) warp_wait(&p_free[i & 1], ((i - 2) >> 1) & 1, p.status, abort);
         if (wact) {
           if (is_row) {
-            uint32_t pk[HK / 2];
-            float ls = 0.f;
+            if (!lo_run) {
+              uint32_t pk[HK / 2];
+              float ls = 0.f;
 #pragma unroll
-            for (int c = 0; c < HK; c += 2) {
-              float p0 = ex2(fmaf(s[c], c2, -m)), p1 = ex2(fmaf(s[c + 1], c2, -m));
-              if (valid < HK) {
-                p0 = c < valid ? p0 : 0.f;
-                p1 = c + 1 < valid ? p1 : 0.f;
+              for (int c = 0; c < HK; c += 2) {
+                float p0 = ex2(fmaf(s[c], c2, -m)), p1 = ex2(fmaf(s[c + 1], c2, -m));
+                if (valid < HK) {
+                  p0 = c < valid ? p0 : 0.f;
+                  p1 = c + 1 < valid ? p1 : 0.f;
+                }
+                // the sum takes the bf16 values P V multiplies, so a row's weights sum to one
+                // up to fp32 rounding (with the lazily raised max a dominant P is not a
+                // power of two, and its bf16 rounding would otherwise shift the row)
+                pk[c / 2] = pack_bf16(p0, p1);
+                ls = add_bf16x2_f32(pk[c / 2], ls);
               }
-              // the sum takes the bf16 values P V multiplies, so a row's weights sum to one
-              // up to fp32 rounding (with the lazily raised max a dominant P is not a
-              // power of two, and its bf16 rounding would otherwise shift the row)
-              pk[c / 2] = pack_bf16(p0, p1);
-              ls = add_bf16x2_f32(pk[c / 2], ls);
-            }
-            l += ls;
-            uint8_t* prow = sP + (i & 1) * C::P_BYTES + row * 128;
+              l += ls;
+              uint8_t* prow = sP + (i & 1) * C::P_BYTES + row * 128;
 #pragma unroll
-            for (int cc = 0; cc < HK / 8; ++cc)
-              *reinterpret_cast<uint4*>(prow + (((half * (HK / 8) + cc) ^ (row & 7)) << 4)) =
-                  make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+              for (int cc = 0; cc < HK / 8; ++cc)
+                *reinterpret_cast<uint4*>(prow + (((half * (HK / 8) + cc) ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            } else {
+              // a short run: P = high + low, both bf16, eight keys at a time
+              float ls = 0.f;
+              uint8_t* prow = sP + (i & 1) * C::P_BYTES + row * 128;
+#pragma unroll
+              for (int cc = 0; cc < HK / 8; ++cc) {
+                uint32_t hk[4], lk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = 8 * cc + 2 * e;
+                  float p0 = ex2(fmaf(s[c], c2, -m)), p1 = ex2(fmaf(s[c + 1], c2, -m));
+                  p0 = c < valid ? p0 : 0.f;
+                  p1 = c + 1 < valid ? p1 : 0.f;
+                  hk[e] = pack_bf16(p0, p1);
+                  lk[e] = pack_bf16(p0 - __uint_as_float(hk[e] << 16), p1 - __uint_as_float(hk[e] & 0xffff0000u));
+                  ls = add_bf16x2_f32(lk[e], add_bf16x2_f32(hk[e], ls));
+                }
+                const int off = ((half * (HK / 8) + cc) ^ (row & 7)) << 4;
+                *reinterpret_cast<uint4*>(prow + off) = make_uint4(hk[0], hk[1], hk[2], hk[3]);
+                *reinterpret_cast<uint4*>(prow + 2 * C::P_BYTES + off) = make_uint4(lk[0], lk[1], lk[2], lk[3]);
+              }
+              l += ls;
+            }
           } else if (is_sc && valid > 0) {
             float* dst = p.part_s +
                          (((static_cast<size_t>(sc_ms) * p.B + b) * p.Hkv + g) * 2 + sc_part) * p.s_stride + j * TK +

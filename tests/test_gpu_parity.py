@@ -39,6 +39,15 @@ CASES = {
     "mha_d64_gamma0": Workload("mha", B=2, Hq=4, Hkv=4, d=64, gamma=0, k=33, n=200, seed=78),
     "k_over_n": Workload("kbig", B=2, Hq=8, Hkv=2, d=64, gamma=2, k=300, n=250, seed=79),
     "short_prefix": Workload("short", B=3, Hq=8, Hkv=4, d=128, gamma=5, k=8, n=None, ragged=(0, 70), seed=80),
+    # more than 32 sequences: the per-warp loops over sequences take several rounds
+    # (narrow combine: few (sequence, KV head) rows; wide: many)
+    "many_seqs_narrow": Workload("b40", B=40, Hq=2, Hkv=1, d=64, gamma=3, k=20, n=None, ragged=(1, 200), seed=81),
+    "many_seqs_wide": Workload("b48", B=48, Hq=32, Hkv=8, d=128, gamma=3, k=16, n=None, ragged=(1, 150), seed=82),
+    # short prefixes whose weight sits on two sinks (same key, different values) and a
+    # few heavy hitters: rounding P to bf16 alone puts one output element past the
+    # tolerance here (1.02 of it, against 0.32 with P's low part)
+    "two_sinks_short": Workload("sinks2", B=24, Hq=16, Hkv=4, d=128, gamma=3, k=6, n=None, ragged=(2, 90),
+                                scheme="heavy", heavy_frac=0.02, sinks=2, u_per_seq=True, seed=85),
 }
 
 
