@@ -16,11 +16,14 @@
  *                         draft tokens appended so far, gathered token by token
  *                         (Vegas §2 step 3; §3 sparse execution, page size one).
  *   vg_iteration          verify -> select -> gamma draft steps, in stream order.
+ *   vg_iteration_plan_*   the same iteration captured once as a CUDA graph and
+ *                         launched step after step.
  *
  * Conventions shared by every call
  *   - All tensor arguments are DEVICE pointers to caller-owned memory, unless a
  *     comment says "host".  The library never allocates, frees or synchronises,
- *     and never keeps a pointer after a call returns.
+ *     and never keeps a pointer after a call returns (except the plans of
+ *     vg_iteration_plan_create, which allocate and keep theirs).
  *   - bf16 is IEEE bfloat16 (uint16 storage); fp32 is IEEE binary32.
  *   - Every call only enqueues work on `stream` (0 = legacy default stream) and
  *     returns.  Arguments are validated on the host before anything is enqueued;
@@ -194,6 +197,38 @@ typedef struct vg_iter_outputs {
 vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in,
                        int32_t k, uint32_t row_mask0, uint32_t row_mask1, vg_iter_outputs* out,
                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * vg_iteration, captured once and launched many times.  A decode loop calls the same
+ * iteration with the same buffers step after step; launching its ~3 + 2*gamma
+ * kernels one by one costs the GPU a fraction of a microsecond each.  A plan records the launch
+ * sequence of one argument set as a CUDA graph, and each launch replays it in a
+ * single call.
+ *
+ * vg_iteration_plan_create: same arguments and validation as vg_iteration (returns
+ *   the same codes, enqueues nothing, writes *plan = NULL on error) plus
+ *   plan (out): receives an opaque handle owned by the caller.
+ *   The plan keeps every pointer it was given, and the values of *dims, *cache, *in
+ *   and *out at creation: each launch reads and writes those same buffers, which
+ *   must stay allocated, at the same addresses, until vg_iteration_plan_destroy.
+ *   Put new inputs in those buffers between launches.  Unlike every other call,
+ *   creating a plan allocates: host memory and the CUDA graph's resources
+ *   (VG_ERR_CUDA if the CUDA runtime refuses).  Do not call it while this
+ *   thread is capturing a stream.  The plan belongs to the current device.
+ * vg_iteration_plan_launch: enqueues one iteration on `stream`, in stream order
+ *   with the work before and after it.  VG_ERR_INVALID_ARG for a NULL plan or a
+ *   current device other than the plan's; VG_ERR_CUDA if the launch fails.  Launches
+ *   of one plan on different streams race on its buffers: order them.
+ * vg_iteration_plan_destroy: frees the plan (NULL is a no-op).  Launches already
+ *   enqueued still complete.
+ */
+typedef struct vg_iteration_plan vg_iteration_plan;
+vg_status vg_iteration_plan_create(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in,
+                                   int32_t k, uint32_t row_mask0, uint32_t row_mask1,
+                                   const vg_iter_outputs* out, void* ws, size_t ws_bytes,
+                                   int32_t* dev_status, vg_iteration_plan** plan);
+vg_status vg_iteration_plan_launch(const vg_iteration_plan* plan, void* stream);
+vg_status vg_iteration_plan_destroy(vg_iteration_plan* plan);
 
 /*
  * vg_sparse_draft_attn without a workspace argument.  This entry point has no

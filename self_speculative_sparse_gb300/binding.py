@@ -23,6 +23,7 @@ VG_ERR_DEVICE_TIMEOUT = -5
 VG_ERR_DEVICE_BOUNDS = -6
 
 ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_sparse_draft_attn", "vg_iteration",
+                "vg_iteration_plan_create", "vg_iteration_plan_launch", "vg_iteration_plan_destroy",
                 "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_last_error", "vg_version",
                 "vg_selftest_lost_wait")
 
@@ -83,6 +84,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_iteration.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), ctypes.POINTER(vg_iter_inputs),
                                i32, u32, u32, ctypes.POINTER(vg_iter_outputs), vp, sz, vp, vp]
     L.vg_iteration.restype = i32
+    L.vg_iteration_plan_create.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache),
+                                           ctypes.POINTER(vg_iter_inputs), i32, u32, u32,
+                                           ctypes.POINTER(vg_iter_outputs), vp, sz, vp, ctypes.POINTER(vp)]
+    L.vg_iteration_plan_create.restype = i32
+    L.vg_iteration_plan_launch.argtypes = [vp, vp]
+    L.vg_iteration_plan_launch.restype = i32
+    L.vg_iteration_plan_destroy.argtypes = [vp]
+    L.vg_iteration_plan_destroy.restype = i32
     L.vg_workspace_size.argtypes = [ctypes.POINTER(vg_dims), i32]
     L.vg_workspace_size.restype = sz
     L.vg_last_error.argtypes = []
@@ -162,6 +171,25 @@ def vg_iteration(dims, cache, inputs: vg_iter_inputs, k, row_mask0, row_mask1, o
     wsb = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
     _check(load().vg_iteration(ctypes.byref(dims), ctypes.byref(cache), ctypes.byref(inputs), k, row_mask0,
                                row_mask1, ctypes.byref(outputs), ptr(ws), wsb, ptr(dev_status), _stream(stream)))
+
+
+def vg_iteration_plan_create(dims, cache, inputs: vg_iter_inputs, k, row_mask0, row_mask1,
+                             outputs: vg_iter_outputs, ws, ws_bytes=None, dev_status=None) -> int:
+    """Capture vg_iteration for these arguments; returns the plan handle (destroy it)."""
+    wsb = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
+    h = ctypes.c_void_p()
+    _check(load().vg_iteration_plan_create(ctypes.byref(dims), ctypes.byref(cache), ctypes.byref(inputs), k,
+                                           row_mask0, row_mask1, ctypes.byref(outputs), ptr(ws), wsb,
+                                           ptr(dev_status), ctypes.byref(h)))
+    return h.value
+
+
+def vg_iteration_plan_launch(plan: int, stream=None) -> None:
+    _check(load().vg_iteration_plan_launch(plan, _stream(stream)))
+
+
+def vg_iteration_plan_destroy(plan: int | None) -> None:
+    _check(load().vg_iteration_plan_destroy(plan))
 
 
 def vg_sparse_draft_attn_noalloc(dims, cache, q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, out,

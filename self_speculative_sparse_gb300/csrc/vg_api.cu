@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <string>
 
 #include "vg.h"
@@ -404,6 +405,98 @@ __global__ void __launch_bounds__(64) lost_wait_kernel(int32_t* status, unsigned
 
 using namespace vg;
 
+namespace vg {
+namespace {
+
+// One vg_iteration call, validated: everything its launch sequence needs.
+struct IterCall {
+  Shape s;
+  const vg_kv_cache* cache;
+  const vg_iter_inputs* in;
+  vg_iter_outputs out;
+  int32_t k;
+  VerifyArgs va;
+  void* ws;
+  WsLayout w;
+  DevInfo di;
+};
+
+vg_status iteration_prepare(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in, int32_t k,
+                            uint32_t row_mask0, uint32_t row_mask1, const vg_iter_outputs* out, void* ws,
+                            size_t ws_bytes, IterCall* c) {
+  vg_status st = check_dims(dims, &c->s);
+  if (st != VG_OK) return st;
+  const Shape& s = c->s;
+  if ((st = check_cache(cache)) != VG_OK) return st;
+  if (!in || !out) return fail(VG_ERR_INVALID_ARG, "inputs and outputs must be non-NULL");
+  if (k < 1) return fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
+  if (row_mask0 == 0) return fail(VG_ERR_INVALID_ARG, "row_mask0 (the selection rows) must be non-zero");
+  if (s.max_len > kTopkMaxLen) return fail(VG_ERR_UNSUPPORTED_SHAPE, "max_len=%d > %d", s.max_len, kTopkMaxLen);
+  c->va = VerifyArgs{in->q_verify, in->k_verify, in->v_verify, in->prefix_len, row_mask0, row_mask1,
+                     out->scores0,  out->scores1,  out->score_stride, out->out_verify};
+  if ((st = check_verify_args(s, c->va)) != VG_OK) return st;
+  if (!out->idx || !out->count || !aligned16(out->idx) || !aligned16(out->count))
+    return fail(VG_ERR_INVALID_ARG, "idx and count must be non-NULL and 16-byte aligned");
+  if ((out->idx1 == nullptr) != (out->count1 == nullptr)) return fail(VG_ERR_INVALID_ARG, "idx1 and count1: both or neither");
+  if (out->idx1 && (!out->scores1 || !aligned16(out->idx1) || !aligned16(out->count1)))
+    return fail(VG_ERR_INVALID_ARG, "idx1 needs scores1 and 16-byte aligned idx1/count1");
+  if (s.gamma > 0) {
+    DraftArgs da{in->q_draft, in->k_draft, in->v_draft, out->idx, out->count, k, in->prefix_len, nullptr, 1,
+                 out->out_draft};
+    if (!in->k_draft || !in->v_draft) return fail(VG_ERR_INVALID_ARG, "k_draft and v_draft must be non-NULL");
+    if ((st = check_draft_args(da)) != VG_OK) return st;
+  }
+  if ((st = device_info(&c->di)) != VG_OK) return st;
+  if ((st = check_ws(s, c->di, ws, ws_bytes, &c->w)) != VG_OK) return st;
+  c->cache = cache;
+  c->in = in;
+  c->out = *out;
+  c->k = k;
+  c->ws = ws;
+  return VG_OK;
+}
+
+// The launch sequence: verify (kernel + combine), the selection(s), gamma draft steps.
+vg_status iteration_enqueue(const IterCall& c, int32_t* dev_status, cudaStream_t strm) {
+  const Shape& s = c.s;
+  const vg_iter_inputs* in = c.in;
+  const vg_iter_outputs& out = c.out;
+  vg_status st = run_verify(s, c.cache, c.va, c.ws, c.w, c.di, dev_status, strm);
+  if (st != VG_OK) return st;
+  if ((st = run_topk(out.scores0, out.score_stride, in->prefix_len, s.B, s.max_len, c.k, out.idx, out.count,
+                     dev_status, strm, true)) != VG_OK)
+    return st;
+  if (out.idx1 && (st = run_topk(out.scores1, out.score_stride, in->prefix_len, s.B, s.max_len, c.k, out.idx1,
+                                 out.count1, dev_status, strm, true)) != VG_OK)
+    return st;
+  const size_t qstep = static_cast<size_t>(s.B) * s.Hq * s.D * 2;
+  const size_t kvstep = static_cast<size_t>(s.B) * s.Hkv * s.D * 2;
+  for (int step = 0; step < s.gamma; ++step) {
+    DraftArgs da{static_cast<const char*>(in->q_draft) + step * qstep,
+                 static_cast<const char*>(in->k_draft) + step * kvstep,
+                 static_cast<const char*>(in->v_draft) + step * kvstep,
+                 out.idx,
+                 out.count,
+                 c.k,
+                 in->prefix_len,
+                 nullptr,
+                 step + 1,
+                 static_cast<char*>(out.out_draft) + step * qstep};
+    if ((st = run_draft(s, c.cache, da, c.ws, c.w, c.di, dev_status, strm, true)) != VG_OK) return st;
+  }
+  return VG_OK;
+}
+
+}  // namespace
+}  // namespace vg
+
+// A captured vg_iteration: the launch sequence of one argument set, as a CUDA graph.
+struct vg_iteration_plan {
+  int device;
+  cudaGraphExec_t exec;
+};
+
+
 extern "C" {
 
 int32_t vg_version(void) { return 100; }
@@ -490,55 +583,79 @@ vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_i
                        uint32_t row_mask0, uint32_t row_mask1, vg_iter_outputs* out, void* ws, size_t ws_bytes,
                        int32_t* dev_status, void* stream) {
   g_err.clear();
-  Shape s;
-  vg_status st = check_dims(dims, &s);
+  IterCall c;
+  vg_status st = iteration_prepare(dims, cache, in, k, row_mask0, row_mask1, out, ws, ws_bytes, &c);
   if (st != VG_OK) return st;
-  if ((st = check_cache(cache)) != VG_OK) return st;
-  if (!in || !out) return fail(VG_ERR_INVALID_ARG, "inputs and outputs must be non-NULL");
-  if (k < 1) return fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
-  if (row_mask0 == 0) return fail(VG_ERR_INVALID_ARG, "row_mask0 (the selection rows) must be non-zero");
-  if (s.max_len > kTopkMaxLen) return fail(VG_ERR_UNSUPPORTED_SHAPE, "max_len=%d > %d", s.max_len, kTopkMaxLen);
-  VerifyArgs va{in->q_verify, in->k_verify, in->v_verify, in->prefix_len, row_mask0, row_mask1,
-                out->scores0,  out->scores1,  out->score_stride, out->out_verify};
-  if ((st = check_verify_args(s, va)) != VG_OK) return st;
-  if (!out->idx || !out->count || !aligned16(out->idx) || !aligned16(out->count))
-    return fail(VG_ERR_INVALID_ARG, "idx and count must be non-NULL and 16-byte aligned");
-  if ((out->idx1 == nullptr) != (out->count1 == nullptr)) return fail(VG_ERR_INVALID_ARG, "idx1 and count1: both or neither");
-  if (out->idx1 && (!out->scores1 || !aligned16(out->idx1) || !aligned16(out->count1)))
-    return fail(VG_ERR_INVALID_ARG, "idx1 needs scores1 and 16-byte aligned idx1/count1");
-  if (s.gamma > 0) {
-    DraftArgs da{in->q_draft, in->k_draft, in->v_draft, out->idx, out->count, k, in->prefix_len, nullptr, 1,
-                 out->out_draft};
-    if (!in->k_draft || !in->v_draft) return fail(VG_ERR_INVALID_ARG, "k_draft and v_draft must be non-NULL");
-    if ((st = check_draft_args(da)) != VG_OK) return st;
+  return iteration_enqueue(c, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+vg_status vg_iteration_plan_create(const vg_dims* dims, const vg_kv_cache* cache, const vg_iter_inputs* in,
+                                   int32_t k, uint32_t row_mask0, uint32_t row_mask1, const vg_iter_outputs* out,
+                                   void* ws, size_t ws_bytes, int32_t* dev_status, vg_iteration_plan** plan) {
+  g_err.clear();
+  if (!plan) return fail(VG_ERR_INVALID_ARG, "plan is NULL");
+  *plan = nullptr;
+  IterCall c;
+  vg_status st = iteration_prepare(dims, cache, in, k, row_mask0, row_mask1, out, ws, ws_bytes, &c);
+  if (st != VG_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  // The sequence is recorded on a private stream.  Relaxed mode: the first launch of a
+  // kernel may raise its shared-memory limit (cudaFuncSetAttribute), which enqueues
+  // nothing and needs no capture.
+  cudaStream_t cs = nullptr;
+  if ((e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess)
+    return cuda_fail(e, "cudaStreamCreateWithFlags");
+  if ((e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed)) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "cudaStreamBeginCapture");
   }
-  DevInfo di;
-  if ((st = device_info(&di)) != VG_OK) return st;
-  WsLayout w;
-  if ((st = check_ws(s, di, ws, ws_bytes, &w)) != VG_OK) return st;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  if ((st = run_verify(s, cache, va, ws, w, di, dev_status, strm)) != VG_OK) return st;
-  if ((st = run_topk(out->scores0, out->score_stride, in->prefix_len, s.B, s.max_len, k, out->idx, out->count,
-                     dev_status, strm, true)) != VG_OK)
-    return st;
-  if (out->idx1 && (st = run_topk(out->scores1, out->score_stride, in->prefix_len, s.B, s.max_len, k, out->idx1,
-                                  out->count1, dev_status, strm, true)) != VG_OK)
-    return st;
-  const size_t qstep = static_cast<size_t>(s.B) * s.Hq * s.D * 2;
-  const size_t kvstep = static_cast<size_t>(s.B) * s.Hkv * s.D * 2;
-  for (int step = 0; step < s.gamma; ++step) {
-    DraftArgs da{static_cast<const char*>(in->q_draft) + step * qstep,
-                 static_cast<const char*>(in->k_draft) + step * kvstep,
-                 static_cast<const char*>(in->v_draft) + step * kvstep,
-                 out->idx,
-                 out->count,
-                 k,
-                 in->prefix_len,
-                 nullptr,
-                 step + 1,
-                 static_cast<char*>(out->out_draft) + step * qstep};
-    if ((st = run_draft(s, cache, da, ws, w, di, dev_status, strm, true)) != VG_OK) return st;
+  st = iteration_enqueue(c, dev_status, cs);
+  std::string enqueue_err = g_err;
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cs, &graph);
+  cudaStreamDestroy(cs);
+  if (st != VG_OK || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (st != VG_OK) {
+      g_err = enqueue_err;
+      return st;
+    }
+    return cuda_fail(e, "cudaStreamEndCapture");
   }
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+  vg_iteration_plan* p = new (std::nothrow) vg_iteration_plan{dev, exec};
+  if (!p) {
+    cudaGraphExecDestroy(exec);
+    return fail(VG_ERR_CUDA, "out of host memory for the plan");
+  }
+  *plan = p;
+  return VG_OK;
+}
+
+vg_status vg_iteration_plan_launch(const vg_iteration_plan* plan, void* stream) {
+  g_err.clear();
+  if (!plan) return fail(VG_ERR_INVALID_ARG, "plan is NULL");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != plan->device)
+    return fail(VG_ERR_INVALID_ARG, "plan was made on device %d, the current device is %d", plan->device, dev);
+  e = cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  return VG_OK;
+}
+
+vg_status vg_iteration_plan_destroy(vg_iteration_plan* plan) {
+  g_err.clear();
+  if (!plan) return VG_OK;
+  const cudaError_t e = cudaGraphExecDestroy(plan->exec);
+  delete plan;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphExecDestroy");
   return VG_OK;
 }
 

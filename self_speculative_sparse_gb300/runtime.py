@@ -67,16 +67,27 @@ class LayerState:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     # --------------------------------------------------------------- calls
-    def iteration(self, stream=None, select_extra: bool = True) -> None:
-        """verify -> select -> gamma draft steps, one C call."""
+    def _iter_args(self, select_extra: bool):
         ins = vb.vg_iter_inputs(vb.ptr(self.q_verify), vb.ptr(self.k_new), vb.ptr(self.v_new), vb.ptr(self.q_draft),
                                 vb.ptr(self.k_draft), vb.ptr(self.v_draft), vb.ptr(self.prefix_len))
         outs = vb.vg_iter_outputs(vb.ptr(self.out_verify), vb.ptr(self.scores0), vb.ptr(self.scores1),
                                   self.score_stride, vb.ptr(self.idx), vb.ptr(self.count),
                                   vb.ptr(self.idx1) if select_extra else None,
                                   vb.ptr(self.count1) if select_extra else None, vb.ptr(self.out_draft))
+        return ins, outs
+
+    def iteration(self, stream=None, select_extra: bool = True) -> None:
+        """verify -> select -> gamma draft steps, one C call."""
+        ins, outs = self._iter_args(select_extra)
         vb.vg_iteration(self.dims, self.cache, ins, self.k, self.mask0, self.mask1, outs, self.ws,
                         dev_status=self.status, stream=stream)
+
+    def plan(self, select_extra: bool = True) -> "IterationPlan":
+        """The iteration on this state's current buffers, captured once (vg_iteration_plan_*)."""
+        ins, outs = self._iter_args(select_extra)
+        h = vb.vg_iteration_plan_create(self.dims, self.cache, ins, self.k, self.mask0, self.mask1, outs, self.ws,
+                                        dev_status=self.status)
+        return IterationPlan(h, [v for v in vars(self).values() if isinstance(v, torch.Tensor)])
 
     def verify(self, stream=None, append: bool = True) -> None:
         vb.vg_verify_attn(self.dims, self.cache, self.q_verify, self.k_new if append else None,
@@ -97,3 +108,35 @@ class LayerState:
 
     def check_status(self) -> int:
         return int(self.status.item())
+
+
+class IterationPlan:
+    """An owned vg_iteration_plan.  It holds the tensors it was captured on, so they stay
+    allocated at the same addresses for as long as the plan lives."""
+
+    def __init__(self, handle: int, tensors: list):
+        self.handle = handle
+        self._tensors = tensors
+
+    def launch(self, stream=None) -> None:
+        if not self.handle:
+            raise RuntimeError("the plan was closed")
+        vb.vg_iteration_plan_launch(self.handle, stream)
+
+    def close(self) -> None:
+        if self.handle:
+            vb.vg_iteration_plan_destroy(self.handle)
+            self.handle = None
+        self._tensors = []
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

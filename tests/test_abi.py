@@ -151,6 +151,27 @@ def test_iteration_rejects_bad_arguments(lib):
                             None, None) == vb.VG_ERR_INVALID_ARG
 
 
+def test_iteration_plan_validates_like_the_call_and_leaves_no_handle(lib):
+    d, c = dims(), cache()
+    ins = vb.vg_iter_inputs(A.addr, A.addr, A.addr, A.addr, A.addr, A.addr, A.addr)
+    outs = vb.vg_iter_outputs(A.addr, A.addr, None, 512, A.addr, A.addr, None, None, A.addr)
+
+    def create(k=16, m0=0x9, m1=0, o=outs, dm=d):
+        h = ctypes.c_void_p(0x1234)
+        code = lib.vg_iteration_plan_create(ctypes.byref(dm) if dm is not None else None, ctypes.byref(c),
+                                            ctypes.byref(ins), k, m0, m1, ctypes.byref(o), vb.ptr(A), 1 << 30,
+                                            None, ctypes.byref(h))
+        return code, h.value
+    for kw in (dict(k=0), dict(m0=0), dict(m1=0x2), dict(dm=None), dict(dm=dims(d=80))):
+        code, h = create(**kw)
+        assert code in (vb.VG_ERR_INVALID_ARG, vb.VG_ERR_UNSUPPORTED_SHAPE), kw
+        assert h is None, kw                                          # *plan = NULL on error
+    assert lib.vg_iteration_plan_create(ctypes.byref(d), ctypes.byref(c), ctypes.byref(ins), 16, 1, 0,
+                                        ctypes.byref(outs), vb.ptr(A), 1 << 30, None, None) == vb.VG_ERR_INVALID_ARG
+    assert lib.vg_iteration_plan_launch(None, None) == vb.VG_ERR_INVALID_ARG
+    assert lib.vg_iteration_plan_destroy(None) == vb.VG_OK
+
+
 def test_workspace_size_rejects_bad_dims(lib):
     assert lib.vg_workspace_size(ctypes.byref(dims(d=80)), 16) == 0
     assert lib.vg_workspace_size(ctypes.byref(dims()), 0) == 0

@@ -84,6 +84,34 @@ def test_iteration_is_deterministic():
                            y.view(torch.int16) if y.dtype == torch.bfloat16 else y), name
 
 
+def test_plan_launches_match_the_call_bit_for_bit():
+    """vg_iteration_plan_*: the captured iteration gives vg_iteration's results, launch
+    after launch, and reads its buffers at launch time (new inputs, new results)."""
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = CASES["batched_b3_n700"]  # two masks: both selections run
+    pool = w.layer_pool(0)
+    names = ("out_verify", "scores0", "scores1", "idx", "count", "idx1", "count1", "out_draft")
+
+    def bits(t):
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+    a, b = LayerState(w, pool), LayerState(w, pool)
+    with b.plan() as plan:
+        for rnd in range(3):
+            if rnd == 2:  # new inputs in the same buffers
+                for st in (a, b):
+                    st.q_verify.copy_(-st.q_verify)
+                    st.q_draft.copy_(st.q_draft.flip(-1))
+            a.iteration()
+            for nm in names:
+                getattr(b, nm).view(torch.uint8).fill_(0xA5)
+            plan.launch()
+            torch.cuda.synchronize()
+            for nm in names:
+                assert torch.equal(bits(getattr(a, nm)), bits(getattr(b, nm))), (rnd, nm)
+    assert a.check_status() == 0 and b.check_status() == 0
+
+
 def test_verify_reads_new_rows_from_cache_when_not_given():
     from self_speculative_sparse_gb300.runtime import LayerState
     w = CASES["llama8b_n1000"]
