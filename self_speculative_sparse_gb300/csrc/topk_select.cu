@@ -9,13 +9,14 @@
 // GB300 design.  One thread-block cluster of up to 16 CTAs per sequence; each CTA
 // keeps its contiguous slice of the scores in shared memory as order-preserving
 // 32-bit keys.  An exact MSB-first radix select (4 passes of 8 bits) finds the
-// k-th largest key: every pass builds per-warp histograms with warp-aggregated
-// increments (one atomic per distinct digit per warp step, eight steps in flight,
-// no contention between warps); each CTA pushes its histogram into every CTA of the
+// k-th largest key: every pass builds per-warp histograms, eight steps in flight and
+// no contention between warps (the first pass, whose top-byte digits pile onto a few
+// sign/exponent values, aggregates equal digits of a warp into one increment; later
+// passes digit inside one top-byte class and increment directly); each CTA pushes its histogram into every CTA of the
 // cluster through distributed shared memory (stores before the cluster barrier, so
 // that after it every CTA sums the cluster's counts from its own shared memory with
-// no remote round trip), and a block-wide scan over the digits lets every CTA pick
-// the same digit.  A final cluster-wide exclusive scan in position order (the CTAs'
+// no remote round trip), and a scan over the digits by the 256 digit threads lets
+// every CTA pick the same digit.  A final cluster-wide exclusive scan in position order (the CTAs'
 // counts pushed the same way) writes the selected positions, taking the needed
 // number of threshold-equal keys from the lowest positions.
 // Everything is integer work: the result is bit-exact and deterministic.
@@ -150,9 +151,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     uint32_t* hw = hist + (tid >> 5) * kBins;
     for (int i = lane; i < kBins; i += 32) hw[i] = 0u;  // this warp's own histogram
     __syncwarp();
-    // warp-aggregated counting, eight independent steps at a time: lanes with the
-    // same digit add once, into their warp's histogram.  Passes 1-2 scan every key
-    // of the slice; passes 3-4 only the warp's list of remaining candidates.
+    // counting into the warp's own histogram, eight independent steps at a time.
+    // Passes 1-2 scan every key of the slice; passes 3-4 only the warp's list of
+    // remaining candidates.
     const bool from_list = lists && pass >= 2 && wcnt <= kListPerWarp;
     const int steps = from_list ? (wcnt + 31) / 32 : rounds;
     for (int rb = 0; rb < steps; rb += 8) {
@@ -174,12 +175,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
         cand[q] = in && (key & pmask) == prefix;
         dg[q] = cand[q] ? ((key >> shift) & 255u) : 0xffffffffu;
       }
-      unsigned peers[8];
+      if (pass == 0) {  // top byte (sign, high exponent bits): few distinct digits, aggregate
+        unsigned peers[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) peers[q] = __match_any_sync(0xffffffffu, dg[q]);
+        for (int q = 0; q < 8; ++q) peers[q] = __match_any_sync(0xffffffffu, dg[q]);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (cand[q] && lane == __ffs(peers[q]) - 1) atomicAdd(&hw[dg[q]], static_cast<uint32_t>(__popc(peers[q])));
+        for (int q = 0; q < 8; ++q)
+          if (cand[q] && lane == __ffs(peers[q]) - 1) atomicAdd(&hw[dg[q]], static_cast<uint32_t>(__popc(peers[q])));
+      } else {  // inside one top-byte class the digits spread: plain increments
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (cand[q]) atomicAdd(&hw[dg[q]], 1u);
+      }
     }
     __syncthreads();
     uint32_t* hb = hall + (pass & 1) * kMaxCluster * kBins;  // [source rank][digit]
@@ -191,51 +198,38 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     }
     cluster.sync();  // the pushes have landed (a buffer is reused two passes on, after
                      // the next pass's sync, so no CTA still reads it)
-    // cluster-wide counts, highest digit first: thread t (< 256) owns digit 255 - t
-    int c4[1];
-    int tsum = 0;
-    {
+    // cluster-wide counts, highest digit first: thread t (< 256) owns digit 255 - t.
+    // The eight warps of digit threads scan their counts, meet once, and each adds the
+    // totals of the warps before it; the thread whose digit holds the remaining-th
+    // largest key of the prefix class publishes it (double-buffered by pass parity, so
+    // a thread still reading one pass's result is never overwritten by the next).
+    int* res = misc + 2 * (pass & 1);
+    if (tid < kBins) {
       int c = 0;
-      if (tid < kBins) {
 #pragma unroll
-        for (int rr = 0; rr < kMaxCluster; ++rr)
-          if (rr < C) c += static_cast<int>(hb[rr * kBins + (kBins - 1 - tid)]);
-      }
-      c4[0] = c;
-      tsum = c;
-    }
-    // block-wide exclusive scan of the per-thread sums (in descending digit order)
-    int incl = tsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) wsum[tid >> 5] = incl;
-    __syncthreads();
-    if (tid < 32) {
-      const int wv = tid < kWarps ? wsum[tid] : 0;
-      int wi = wv;
+      for (int rr = 0; rr < kMaxCluster; ++rr)
+        if (rr < C) c += static_cast<int>(hb[rr * kBins + (kBins - 1 - tid)]);
+      int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += t;
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
       }
-      if (tid < kWarps) wsum[tid] = wi - wv;
+      if (lane == 31) wsum[tid >> 5] = incl;
+      asm volatile("bar.sync 1, %0;" ::"n"(kBins) : "memory");
+      int before = 0;
+      for (int w = 0; w < (tid >> 5); ++w) before += wsum[w];
+      const int run = before + incl - c;
+      if (run < remaining && remaining <= run + c) {
+        res[0] = kBins - 1 - tid;
+        res[1] = run;
+      }
     }
     __syncthreads();
-    // the digit whose keys hold the remaining-th largest of the prefix class
-    const int run = wsum[tid >> 5] + incl - tsum;
-    if (tid < kBins && run < remaining && remaining <= run + c4[0]) {
-      misc[0] = kBins - 1 - tid;
-      misc[1] = run;
-    }
-    __syncthreads();
-    const int digit = misc[0];
-    remaining -= misc[1];
+    const int digit = res[0];
+    remaining -= res[1];
     prefix |= static_cast<uint32_t>(digit) << shift;
     pmask |= 255u << shift;
-    __syncthreads();
     if (lists && pass == 1) {  // the keys still matching the 16-bit prefix, in this warp's list
       const unsigned lt = (1u << lane) - 1u;
       for (int rr = 0; rr < rounds; ++rr) {
