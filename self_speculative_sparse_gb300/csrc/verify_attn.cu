@@ -594,7 +594,7 @@ constexpr int kCombineWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(const VerifyParams p) {
   constexpr int PER = D / 32;  // elements of a row per lane
-  constexpr int NB = 8;        // partial rows per round of loads
+  constexpr int NB = D == 128 ? 4 : 8;  // partial rows per round of loads (two rounds in registers)
   __shared__ float lgs[kCombineWarps][16];               // a warp's causal logits (log2 units)
   __shared__ __align__(16) __nv_bfloat16 kvs[2][16][D];  // the verify rows' keys and values
   pdl_launch_dependents();  // the selection kernel may start its prologue
