@@ -417,6 +417,46 @@ def run_ours(args, rank, local, world):
     t_verify = ph[0].elapsed_time(ph[1]) * 1e3 / args.steps
     t_select = ph[1].elapsed_time(ph[2]) * 1e3 / args.steps
     t_draft = ph[2].elapsed_time(ph[3]) * 1e3 / args.steps
+    # ---- K steps launched eagerly (no graph): one vg_iteration call per step (the
+    # model's per-layer calls for the multi-layer workload); the mean from two events
+    # around them, the spread from a second pass with an event between steps
+    def eager_step(i):
+        if multi:
+            step(i)
+        else:
+            states[i % ncopy].iteration(stream=stream, select_extra=False)
+
+    torch.cuda.synchronize()
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ee[0].record(stream)
+    for i in range(args.steps):
+        eager_step(args.warmup + i)
+    ee[1].record(stream)
+    torch.cuda.synchronize()
+    eager_mean = ee[0].elapsed_time(ee[1]) * 1e3 / args.steps
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    es[0].record(stream)
+    for i in range(args.steps):
+        eager_step(args.warmup + i)
+        es[i + 1].record(stream)
+    torch.cuda.synchronize()
+    eager_steps = sorted(es[i].elapsed_time(es[i + 1]) * 1e3 for i in range(args.steps))
+
+    def pct(v, q):
+        return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+    # ---- secondary: the draft phase with its gathered entries warm in L2 (K draft
+    # phases on one cache copy), where the headline reads every step cold
+    draft_warm = None
+    if not multi:
+        g_dw = capture(lambda: [draft_phase(states[0]) for _ in range(args.steps)])
+        g_dw.replay()
+        torch.cuda.synchronize()
+        ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ew[0].record(stream)
+        g_dw.replay()
+        ew[1].record(stream)
+        torch.cuda.synchronize()
+        draft_warm = ew[0].elapsed_time(ew[1]) * 1e3 / args.steps / max(1, w.gamma)
     # ---- cost of the fused logit aggregation: the verify call with no scores, with the
     # Collect-2-Query rows and with all rows (same rotation, K back-to-back calls)
     R = w.gamma + 1
@@ -533,6 +573,12 @@ def run_ours(args, rank, local, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_bytes_per_iteration": nbytes["verify"] + nbytes["draft"],
         "kv_gbs": kv_gbs, "kv_pct_of_hbm": 100.0 * kv_gbs / peaks["hbm_gbs"],
+        "eager_launches_us": {"mean": eager_mean, "p10": pct(eager_steps, 0.1), "p50": pct(eager_steps, 0.5),
+                              "p90": pct(eager_steps, 0.9),
+                              "note": "per rank, no CUDA graph: vg_iteration per step (its kernels launched one "
+                                      "by one; the multi-layer workload: its per-layer calls in the model's "
+                                      "order); percentiles over steps timed with an event between steps"},
+        "draft_step_l2_warm_us": draft_warm,
         "phases_us": {"verify_call": t_verify, "select": t_select, "draft_gamma_steps": t_draft,
                       "per_draft_step": t_draft / max(1, w.gamma)},
         "phases_note": "sums over the layers of one step" if multi else "one layer",
