@@ -168,11 +168,36 @@ def measured_peaks() -> dict:
 VERIFY_SOURCES = ("verify_attn.cu", "attn_frag.cuh", "vg_common.cuh", "vg_internal.h")
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and character
+    literals kept as they are), so that editing a comment leaves the code's hash."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(ln.rstrip() for ln in "".join(out).split("\n") if ln.strip())
+
+
 def verify_source_sha() -> str:
-    """sha256 over the sources the verify kernel is compiled from."""
+    """sha256 over the code (comments left out) the verify kernel is compiled from."""
     h = hashlib.sha256()
     for f in VERIFY_SOURCES:
-        h.update(open(os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", f), encoding="utf-8").read()
+        h.update(strip_c_comments(src).encode())
     return h.hexdigest()
 
 

@@ -25,9 +25,10 @@
 // sum are per thread; the two halves of a row agree on the tile max through shared
 // memory; the running max is raised only when a tile exceeds it by more than 2^8,
 // after which the row's O is rescaled in tensor memory), and writes its half row of
-// P (bf16) to shared memory for the P V product.  When the query and score rows fit in
-// 64, the MMAs use M = 64, which halves the Q and P buffers and leaves room for a fifth
-// stage.  A score-row
+// P (bf16) to shared memory for the P V product; in runs of a short prefix it also
+// writes P's low part, P - bf16(P), which a second P V product adds in.  When the
+// query and score rows fit in 64, the MMAs use M = 64, which halves the Q and P
+// buffers and leaves room for more stages.  A score-row
 // thread's S row is already the summed logit q_sum . k of each key of the tile
 // (high part plus low part), so the aggregation costs two rows of the same MMA and
 // no shuffles; the cache is read exactly once.  Each contiguous run of tiles of one
