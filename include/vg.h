@@ -199,11 +199,13 @@ vg_status vg_iteration(const vg_dims* dims, const vg_kv_cache* cache, const vg_i
                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
- * vg_iteration, captured once and launched many times.  A decode loop calls the same
- * iteration with the same buffers step after step; launching its ~3 + 2*gamma
- * kernels one by one costs the GPU a fraction of a microsecond each.  A plan records the launch
- * sequence of one argument set as a CUDA graph, and each launch replays it in a
- * single call.
+ * vg_iteration (Vegas §2 steps 1-3), captured once and launched many times.  This
+ * has no counterpart in the paper, which runs inside a serving framework's loop.  A
+ * decode loop calls the same iteration with the same buffers step after step;
+ * launching its ~3 + 2*gamma kernels one by one costs the GPU a fraction of a
+ * microsecond each.  A plan records the launch sequence of one argument set as a CUDA
+ * graph, and each launch replays it in a single call, with the same results as
+ * vg_iteration on the buffers' contents at launch time.
  *
  * vg_iteration_plan_create: same arguments and validation as vg_iteration (returns
  *   the same codes, enqueues nothing, writes *plan = NULL on error) plus
