@@ -2,8 +2,8 @@
 
 Small cases that the oracle finishes in seconds but that still span several
 tiles, ragged tails, empty and one-entry prefixes, every m-tile count of the
-verify kernel (G*(gamma+1) = 16, 28, 32, 48, 64), both head dims, gamma = 0 and
-k >= n.
+verify kernel (G*(gamma+1) = 16, 28, 32, 48, 64), both head dims (both MMA row counts
+at each), gamma = 0 and k >= n.
 """
 import numpy as np
 import pytest
@@ -36,6 +36,7 @@ CASES = {
     "long70b_n2100": scaled(W["long70b"], n=2100),
     "ragged_b6": scaled(W["loop32"], B=6, layers=1, ragged=(1, 1500)),
     "g16_m64": Workload("g16", B=2, Hq=16, Hkv=1, d=128, gamma=3, k=100, n=777, seed=77),
+    "g16_m64_d64": Workload("g16d64", B=2, Hq=16, Hkv=1, d=64, gamma=3, k=100, n=777, seed=84),
     "mha_d64_gamma0": Workload("mha", B=2, Hq=4, Hkv=4, d=64, gamma=0, k=33, n=200, seed=78),
     "k_over_n": Workload("kbig", B=2, Hq=8, Hkv=2, d=64, gamma=2, k=300, n=250, seed=79),
     "short_prefix": Workload("short", B=3, Hq=8, Hkv=4, d=128, gamma=5, k=8, n=None, ragged=(0, 70), seed=80),
