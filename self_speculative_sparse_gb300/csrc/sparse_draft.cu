@@ -407,9 +407,8 @@ cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl) {
   if (p.Hkv <= 8) {
     if (p.D == 64) return launch_draft_t<64, 8>(p, stream, pdl);
     if (p.D == 128) return launch_draft_t<128, 8>(p, stream, pdl);
-  } else {
-    if (p.D == 64) return launch_draft_t<64, 16>(p, stream, pdl);
-    if (p.D == 128) return launch_draft_t<128, 16>(p, stream, pdl);
+  } else if (p.D == 64) {  // (more than 8 KV heads at d = 128 exceed a 1024-element page)
+    return launch_draft_t<64, 16>(p, stream, pdl);
   }
   return cudaErrorInvalidValue;
 }

@@ -336,11 +336,17 @@ vg_status check_draft_args(const DraftArgs& a) {
   return VG_OK;
 }
 
-vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, void* ws, const WsLayout& w,
-                    const DevInfo& di, int32_t* dev_status, cudaStream_t stream, bool pdl) {
+// One token's K and V pages of every KV head are staged whole in shared memory.
+vg_status check_draft_smem(const Shape& s, const DevInfo& di) {
   if (draft_smem_bytes(s.D, s.Hkv) > di.smem_optin)
     return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d needs more shared memory than a CTA has",
                 s.Hkv * s.D);
+  return VG_OK;
+}
+
+vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, void* ws, const WsLayout& w,
+                    const DevInfo& di, int32_t* dev_status, cudaStream_t stream, bool pdl) {
+  if (const vg_status st = check_draft_smem(s, di); st != VG_OK) return st;
   DraftParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
@@ -447,6 +453,8 @@ vg_status iteration_prepare(const vg_dims* dims, const vg_kv_cache* cache, const
     if ((st = check_draft_args(da)) != VG_OK) return st;
   }
   if ((st = device_info(&c->di)) != VG_OK) return st;
+  // (checked here, not first in the draft launches: an error must leave nothing enqueued)
+  if (s.gamma > 0 && (st = check_draft_smem(s, c->di)) != VG_OK) return st;
   if ((st = check_ws(s, c->di, ws, ws_bytes, &c->w)) != VG_OK) return st;
   c->cache = cache;
   c->in = in;

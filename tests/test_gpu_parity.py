@@ -44,6 +44,11 @@ CASES = {
     # (narrow combine: few (sequence, KV head) rows; wide: many)
     "many_seqs_narrow": Workload("b40", B=40, Hq=2, Hkv=1, d=64, gamma=3, k=20, n=None, ragged=(1, 200), seed=81),
     "many_seqs_wide": Workload("b48", B=48, Hq=32, Hkv=8, d=128, gamma=3, k=16, n=None, ragged=(1, 150), seed=82),
+    # 16 KV heads at d = 64: the draft kernel's 16-consumer-warp form
+    "hkv16_d64": Workload("h16", B=3, Hq=32, Hkv=16, d=64, gamma=3, k=40, n=None, ragged=(1, 400), seed=86),
+    # many (sequence, KV head) rows at d = 64: the wide verify combine at that head dim
+    "many_seqs_wide_d64": Workload("w64", B=80, Hq=8, Hkv=4, d=64, gamma=3, k=8, n=None, ragged=(1, 100),
+                                   seed=87),
     # short prefixes whose weight sits on two sinks (same key, different values) and a
     # few heavy hitters: rounding P to bf16 alone puts one output element past the
     # tolerance here (1.02 of it, against 0.32 with P's low part)
@@ -111,6 +116,48 @@ def test_plan_launches_match_the_call_bit_for_bit():
             for nm in names:
                 assert torch.equal(bits(getattr(a, nm)), bits(getattr(b, nm))), (rnd, nm)
     assert a.check_status() == 0 and b.check_status() == 0
+
+
+def test_iteration_refuses_an_unstageable_draft_shape_before_enqueueing_anything():
+    """16 KV heads at d = 128 leave no room to stage a token's pages for the draft: the
+    call (and a plan) must refuse before the verify and selection are enqueued."""
+    import ctypes
+    from self_speculative_sparse_gb300 import binding as vb
+    B, Hq, Hkv, d, gamma, n, k = 1, 16, 16, 128, 1, 64, 8
+    R, dev = gamma + 1, "cuda"
+    dims = vb.vg_dims(B=B, H_q=Hq, H_kv=Hkv, d=d, gamma=gamma, max_len=n, scale=0.0)
+    slots = n + R + 16
+    K = torch.zeros(slots, Hkv, d, dtype=torch.bfloat16, device=dev)
+    V = torch.zeros_like(K)
+    off = torch.zeros(B, dtype=torch.int64, device=dev)
+    cache = vb.vg_kv_cache(vb.ptr(K), vb.ptr(V), vb.ptr(off), slots)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    q, kn, vn = torch.zeros(B, R, Hq, d, **bf), torch.zeros(B, R, Hkv, d, **bf), torch.zeros(B, R, Hkv, d, **bf)
+    qd, kd, vd = torch.zeros(gamma, B, Hq, d, **bf), torch.zeros(gamma, B, Hkv, d, **bf), torch.zeros(gamma, B, Hkv, d, **bf)
+    plen = torch.full((B,), n, dtype=torch.int32, device=dev)
+    scores = torch.full((B, n), 7.0, device=dev)
+    out = torch.full((B, R, Hq, d), 3.0, **bf)
+    idx = torch.full((B, k), 5, dtype=torch.int32, device=dev)
+    cnt = torch.full((B,), 5, dtype=torch.int32, device=dev)
+    outd = torch.full((gamma, B, Hq, d), 3.0, **bf)
+    wsb = vb.vg_workspace_size(dims, k)
+    assert wsb > 0
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ins = vb.vg_iter_inputs(vb.ptr(q), vb.ptr(kn), vb.ptr(vn), vb.ptr(qd), vb.ptr(kd), vb.ptr(vd), vb.ptr(plen))
+    outs = vb.vg_iter_outputs(vb.ptr(out), vb.ptr(scores), None, n, vb.ptr(idx), vb.ptr(cnt), None, None,
+                              vb.ptr(outd))
+    lib = vb.load()
+    mask = 1 | (1 << gamma)
+    code = lib.vg_iteration(ctypes.byref(dims), ctypes.byref(cache), ctypes.byref(ins), k, mask, 0,
+                            ctypes.byref(outs), vb.ptr(ws), wsb, None, None)
+    h = ctypes.c_void_p(0x1234)
+    code_plan = lib.vg_iteration_plan_create(ctypes.byref(dims), ctypes.byref(cache), ctypes.byref(ins), k, mask,
+                                             0, ctypes.byref(outs), vb.ptr(ws), wsb, None, ctypes.byref(h))
+    torch.cuda.synchronize()
+    assert code == vb.VG_ERR_UNSUPPORTED_SHAPE and code_plan == vb.VG_ERR_UNSUPPORTED_SHAPE
+    assert h.value is None
+    assert bool((scores == 7.0).all()) and bool((out.float() == 3.0).all()) and bool((outd.float() == 3.0).all())
+    assert bool((idx == 5).all()) and bool((cnt == 5).all()) and bool((K == 0).all())
 
 
 def test_verify_reads_new_rows_from_cache_when_not_given():
