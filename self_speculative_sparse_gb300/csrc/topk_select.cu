@@ -20,6 +20,8 @@
 // counts pushed the same way) writes the selected positions, taking the needed
 // number of threshold-equal keys from the lowest positions.
 // Everything is integer work: the result is bit-exact and deterministic.
+#include <atomic>
+
 #include <cooperative_groups.h>
 
 #include "vg_common.cuh"
@@ -334,14 +336,14 @@ cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, b
   cudaError_t e = ensure_smem<topk_kernel>(smem);
   if (e != cudaSuccess) return e;
   if (cluster > 8) {
-    static int nonportable[64] = {0};
+    static std::atomic<int> nonportable[64] = {};  // (set once per device; any thread)
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!nonportable[dev]) {
+    if (!nonportable[dev].load(std::memory_order_acquire)) {
       e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
-      nonportable[dev] = 1;
+      nonportable[dev].store(1, std::memory_order_release);
     }
   }
   cudaLaunchConfig_t cfg = {};
