@@ -160,6 +160,28 @@ def test_iteration_refuses_an_unstageable_draft_shape_before_enqueueing_anything
     assert bool((idx == 5).all()) and bool((cnt == 5).all()) and bool((K == 0).all())
 
 
+def test_draft_over_the_whole_prefix_equals_verify_row_zero():
+    """Two kernels against each other: with k >= n the selection is the whole prefix, and
+    a draft token equal to verify row 0 (same q, k, v) attends exactly what that row
+    attends - the prefix and itself.  Each path is within the oracle tolerance, so they
+    agree within twice that."""
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = Workload("xk", B=3, Hq=8, Hkv=2, d=128, gamma=1, k=2048, n=None, ragged=(1, 1500), seed=88)
+    st = LayerState(w, w.layer_pool(0))
+    st.q_draft[0].copy_(st.q_verify[:, 0])
+    st.k_draft[0].copy_(st.k_new[:, 0])
+    st.v_draft[0].copy_(st.v_new[:, 0])
+    st.iteration(select_extra=False)
+    torch.cuda.synchronize()
+    assert st.check_status() == 0
+    n = st.prefix_len.cpu().numpy()
+    assert np.array_equal(st.count.cpu().numpy(), n)          # everything selected
+    a = st.out_draft[0].float().cpu().numpy()
+    b = st.out_verify[:, 0].float().cpu().numpy()
+    lim = 4e-3 + 2e-2 * np.abs(b)
+    assert np.all(np.abs(a - b) <= lim), float(np.max(np.abs(a - b) - lim))
+
+
 def test_verify_reads_new_rows_from_cache_when_not_given():
     from self_speculative_sparse_gb300.runtime import LayerState
     w = CASES["llama8b_n1000"]
