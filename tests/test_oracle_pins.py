@@ -289,6 +289,40 @@ def test_widen_bf16_exact():
     assert got[5] == float(np.float32(3.3895313892515355e38))
 
 
+# ------------------------------------------------------------ selection overlap
+# Vegas §2.B (Collect-2-Query, observation): the entries selected from different
+# rows of the draft chain largely coincide.  The overlap of two size-k selections is
+# the fraction of one selection that the other also holds, |A ∩ B| / k.
+def test_overlap_hand_computed_cases():
+    a = np.array([0, 2, 4, 6])
+    b = np.array([2, 3, 4, 5])
+    assert oracle.selection_overlap(a, b, 4) == 0.5                       # {2, 4} of 4
+    assert oracle.selection_overlap(a, a, 4) == 1.0
+    assert oracle.selection_overlap(a, np.array([1, 3, 5, 7]), 4) == 0.0  # disjoint
+    assert oracle.selection_overlap(np.array([9]), np.array([9]), 1) == 1.0
+    assert oracle.selection_overlap(np.array([], dtype=np.int64), np.array([], dtype=np.int64), 0) == 1.0
+
+
+def test_overlap_against_set_intersection_and_symmetry():
+    r = np.random.default_rng(17)
+    for _ in range(200):
+        n = int(r.integers(1, 40))
+        k = int(r.integers(1, n + 1))
+        a = np.sort(r.choice(n, size=k, replace=False))
+        b = np.sort(r.choice(n, size=k, replace=False))
+        want = len(set(a.tolist()) & set(b.tolist())) / k
+        assert oracle.selection_overlap(a, b, k) == want
+        assert oracle.selection_overlap(b, a, k) == want
+
+
+def test_overlap_of_selections_with_k_at_least_n_is_one():
+    # both masks select every prefix entry when k >= n, whatever their scores
+    q, K = _rand(4, 8, 16), _rand(9, 2, 16)
+    ta = oracle.select_topk(oracle.aggregated_scores(q, K, [0, 3]), 20)
+    tb = oracle.select_topk(oracle.aggregated_scores(q, K, [0, 1, 2, 3]), 20)
+    assert oracle.selection_overlap(ta, tb, min(20, 9)) == 1.0
+
+
 # ------------------------------------------------------------ planted mistakes
 def _pin_errors(mod):
     """Discrepancies of the pins above for a (possibly mutated) oracle module."""
@@ -314,12 +348,13 @@ def _pin_errors(mod):
     dense = mod.verify_attention(q, K, V, kn, vn)[2]
     sparse = mod.draft_step(q[2], K, V, np.arange(n), kn[:3], vn[:3])
     errs["k_eq_n"] = np.abs(dense - sparse).max()
+    errs["overlap"] = abs(mod.selection_overlap(np.array([0, 2, 4, 6]), np.array([2, 3, 4, 5]), 4) - 0.5)
     return errs
 
 
 def _caught(errs):
     return (errs["sdpa"] > 1e-9 or errs["linearity"] > 1e-9 or errs["worked"] > 1e-9
-            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9)
+            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9 or errs["overlap"] > 0)
 
 
 def test_unmutated_oracle_passes_every_pin():
@@ -334,6 +369,8 @@ MUTANTS = {
     "select the smallest": ("select_topk", None, None),
     "scores skip the last row": ("aggregated_scores", None, None),
     "draft drops the current token": ("draft_step", None, None),
+    "overlap over the union (Jaccard)": ("selection_overlap", None, None),
+    "overlap over the larger total": ("selection_overlap", None, None),
 }
 
 
@@ -384,6 +421,15 @@ def _mutant(name):
         def draft_step(q, K, V, idx, tail_K, tail_V, scale=None):
             return ov.draft_step(q, K, V, idx, tail_K[:-1], tail_V[:-1], scale)
         m.draft_step = draft_step
+    elif name == "overlap over the union (Jaccard)":
+        def selection_overlap(a, b, k):
+            u = np.union1d(a, b)
+            return len(np.intersect1d(a, b)) / float(len(u)) if len(u) else 1.0
+        m.selection_overlap = selection_overlap
+    elif name == "overlap over the larger total":
+        def selection_overlap(a, b, k):
+            return len(np.intersect1d(a, b)) / float(len(a) + len(b)) if k > 0 else 1.0
+        m.selection_overlap = selection_overlap
     return m
 
 
