@@ -243,8 +243,10 @@ vg_status vg_iteration_plan_destroy(vg_iteration_plan* plan);
  *   - It allocates and frees nothing.
  *   - Dimensions whose draft scratch exceeds 8 MiB are rejected with
  *     VG_ERR_WORKSPACE (for 152 SMs: about H_q * (152 + B) * (d + 2) * 4 bytes).
- *   - The first call on each device looks up the area's device address; make that
- *     first call before any stream capture.
+ *   - The first call on each device looks up the area's device address and keeps
+ *     it for the life of the process; make that first call before any stream
+ *     capture, and do not reset a device (cudaDeviceReset) while the library is
+ *     loaded, since the kept address would then be stale.
  *   - All calls share the one area, which keeps the last call's contents (nothing
  *     in it needs to start at zero).  Calls that may overlap on the GPU - on
  *     different streams, or from different host threads - race on it; order them.

@@ -39,7 +39,6 @@
 // (deterministic, no atomics).
 #include <cstdio>
 
-#include "attn_frag.cuh"
 #include "vg_common.cuh"
 #include "vg_internal.h"
 

@@ -336,8 +336,18 @@ vg_status check_draft_args(const DraftArgs& a) {
   return VG_OK;
 }
 
-// One token's K and V pages of every KV head are staged whole in shared memory.
+// One token's K and V pages of every KV head are staged whole in shared memory, which
+// the draft kernels are built for up to 1024 elements a page (checked on the host,
+// before any device query, so an unsupported shape never gets as far as a launch).
+vg_status check_draft_page(const Shape& s) {
+  if (s.Hkv * s.D > 1024)
+    return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d > 1024 (one token's page is staged whole)",
+                s.Hkv * s.D);
+  return VG_OK;
+}
+
 vg_status check_draft_smem(const Shape& s, const DevInfo& di) {
+  if (const vg_status st = check_draft_page(s); st != VG_OK) return st;
   if (draft_smem_bytes(s.D, s.Hkv) > di.smem_optin)
     return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d needs more shared memory than a CTA has",
                 s.Hkv * s.D);
@@ -451,6 +461,7 @@ vg_status iteration_prepare(const vg_dims* dims, const vg_kv_cache* cache, const
                  out->out_draft};
     if (!in->k_draft || !in->v_draft) return fail(VG_ERR_INVALID_ARG, "k_draft and v_draft must be non-NULL");
     if ((st = check_draft_args(da)) != VG_OK) return st;
+    if ((st = check_draft_page(s)) != VG_OK) return st;
   }
   if ((st = device_info(&c->di)) != VG_OK) return st;
   // (checked here, not first in the draft launches: an error must leave nothing enqueued)
@@ -580,6 +591,7 @@ vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, co
   if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
   DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
   if ((st = check_draft_args(a)) != VG_OK) return st;
+  if ((st = check_draft_page(s)) != VG_OK) return st;
   DevInfo di;
   if ((st = device_info(&di)) != VG_OK) return st;
   WsLayout w;
@@ -713,6 +725,7 @@ vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* c
   if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
   DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
   if ((st = check_draft_args(a)) != VG_OK) return st;
+  if ((st = check_draft_page(s)) != VG_OK) return st;
   DevInfo di;
   if ((st = device_info(&di)) != VG_OK) return st;
   const WsLayout w = ws_layout(s, di.sms);

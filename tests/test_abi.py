@@ -184,3 +184,28 @@ def test_lost_wait_self_test_validates_its_arguments_on_the_host(lib):
     assert lib.vg_selftest_lost_wait(1000, None, None, None) == vb.VG_ERR_INVALID_ARG
     assert lib.vg_selftest_lost_wait(1000, Buf().addr + 2, None, None) == vb.VG_ERR_INVALID_ARG
     assert lib.vg_selftest_lost_wait(1000, Buf().addr, Buf().addr + 4, None) == vb.VG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("H_kv", [9, 12, 14, 16])
+def test_draft_pages_above_1024_elements_are_refused_before_any_device_query(lib, H_kv):
+    """One token's K and V pages of every KV head are staged whole; at d = 128 more than
+    8 KV heads exceed that.  The draft call, its no-allocation form and the iteration
+    (and a plan of it) refuse such a shape on the host, before any CUDA call, so on a
+    machine without a GPU the answer is VG_ERR_UNSUPPORTED_SHAPE, not VG_ERR_CUDA."""
+    d, c = dims(B=1, H_q=H_kv, H_kv=H_kv, d=128, gamma=1, max_len=64), cache()
+    code = lib.vg_sparse_draft_attn(ctypes.byref(d), ctypes.byref(c), vb.ptr(A), vb.ptr(A), vb.ptr(A), vb.ptr(A),
+                                    vb.ptr(A), 8, vb.ptr(A), vb.ptr(A), vb.ptr(A), vb.ptr(A), 1 << 30, None, None)
+    assert code == vb.VG_ERR_UNSUPPORTED_SHAPE
+    code = lib.vg_sparse_draft_attn_noalloc(ctypes.byref(d), ctypes.byref(c), vb.ptr(A), vb.ptr(A), vb.ptr(A),
+                                            vb.ptr(A), vb.ptr(A), 8, vb.ptr(A), vb.ptr(A), vb.ptr(A), None, None)
+    assert code == vb.VG_ERR_UNSUPPORTED_SHAPE
+    ins = vb.vg_iter_inputs(A.addr, A.addr, A.addr, A.addr, A.addr, A.addr, A.addr)
+    outs = vb.vg_iter_outputs(A.addr, A.addr, None, 64, A.addr, A.addr, None, None, A.addr)
+    assert lib.vg_iteration(ctypes.byref(d), ctypes.byref(c), ctypes.byref(ins), 8, 0x3, 0, ctypes.byref(outs),
+                            vb.ptr(A), 1 << 30, None, None) == vb.VG_ERR_UNSUPPORTED_SHAPE
+    h = ctypes.c_void_p(0x1234)
+    assert lib.vg_iteration_plan_create(ctypes.byref(d), ctypes.byref(c), ctypes.byref(ins), 8, 0x3, 0,
+                                        ctypes.byref(outs), vb.ptr(A), 1 << 30, None,
+                                        ctypes.byref(h)) == vb.VG_ERR_UNSUPPORTED_SHAPE
+    assert h.value is None
+    assert "1024" in lib.vg_last_error().decode()

@@ -5,7 +5,8 @@ cudaMalloc there can synchronise the device and stall other streams, or the host
 simply has no workspace to offer.  vg_sparse_draft_attn_noalloc serves them from a
 scratch area built into the library.  These tests call it through the C ABI, twice
 in a row, and compare each result with vg_sparse_draft_attn (the workspace entry
-point) on the same inputs; and they check that dimensions too large for the
+point) on the same inputs: both run the same kernels in the same order, so the
+outputs must agree bit for bit.  They also check that dimensions too large for the
 built-in area are refused before anything runs.
 """
 import pytest
@@ -27,7 +28,6 @@ def test_noalloc_draft_step_matches_the_workspace_entry_point_twice():
     import synth
     from self_speculative_sparse_gb300 import binding as vb
     from self_speculative_sparse_gb300.runtime import LayerState
-    from tests.parity import assert_attn_close, bf16_to_f64
 
     w = synth.scaled(synth.WORKLOADS["llama8b"], B=2, n=3000, k=256)
     st = LayerState(w, w.layer_pool(0))
@@ -44,14 +44,14 @@ def test_noalloc_draft_step_matches_the_workspace_entry_point_twice():
                                         st.count, st.k, st.prefix_len, tl, got, dev_status=st.status)
         torch.cuda.synchronize()
         assert st.check_status() == 0
-        assert_attn_close(bf16_to_f64(got), bf16_to_f64(ref), f"no-allocation draft step, call {s + 1}")
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"no-allocation draft step, call {s + 1}"
 
 
 def test_noalloc_refuses_dimensions_beyond_its_scratch():
     from self_speculative_sparse_gb300 import binding as vb
 
     t = torch.zeros(1024, dtype=torch.int64, device="cuda")
-    dims = vb.make_dims(1024, 128, 16, 128, 3, 4096)  # draft scratch far above the built-in 8 MiB
+    dims = vb.make_dims(1024, 128, 8, 128, 3, 4096)  # draft scratch far above the built-in 8 MiB
     cache = vb.make_cache(t, t, t, capacity_slots=16)
     with pytest.raises(vb.VgError) as e:
         vb.vg_sparse_draft_attn_noalloc(dims, cache, t, None, None, t, t, 16, t, t, t)
