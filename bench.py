@@ -1,19 +1,24 @@
 """Benchmark of the Vegas hot path: one verify + select + gamma-step sparse-draft iteration.
 
-Default workload: one Llama-3-8B-shaped layer (B=1, H_q=32, H_kv=8, d=128,
-n=32768, gamma=7, k=2048, Collect-2-Query), synthetic heavy-hitter data.
+Default workload: the full iteration loop, 32 layers of Llama-3-8B-shaped heads
+(H_q=32, H_kv=8, d=128) over B=8 sequences with ragged prefix lengths
+n ~ U[4096, 65536], gamma=6, k=2048, Collect-2-Query selection; synthetic
+heavy-hitter data.  The same line carries per-phase figures of the one-layer
+workloads (llama8b n=32768; long70b n=131072; batched B=16 n=16384).
 
 Timing discipline
-  * the KV cache is replicated into enough copies that all of them together are
-    larger than 4x L2; step i verifies + selects on copy i mod C and runs the gamma
-    draft steps on copy (i + C/2) mod C, so every kernel reads HBM cold and the
-    draft never profits from the verify pass that precedes it.  The draft uses
-    that copy's own selection (made earlier on identical data), which is the
-    method's order anyway: a draft phase follows the previous verification.
+  * Multi-layer workload: every layer stays resident (each is far larger than L2)
+    and a step runs the model's order: verify and select on every layer, then each
+    draft step over every layer.  One-layer workloads: the KV cache is replicated
+    into enough copies that all of them together exceed 4x L2; step i verifies +
+    selects on copy i mod C and runs the gamma draft steps on copy (i + C/2) mod C,
+    so every kernel reads HBM cold and the draft never profits from the verify pass
+    before it (the draft uses that copy's own earlier selection, the method's order).
   * W untimed warm-up steps, then K steps between CUDA events on the launching
     stream, bracketed by a barrier and device synchronisation; rank 0 prints the
-    max over ranks.  Per-phase events inside the timed region give the verify
-    call's duration for the roofline figure.
+    max over ranks.  Per-phase graphs (K verify calls, K selections, K draft phases
+    on the same rotation) give the three roofline fractions: the verify call, the
+    fused verify+select pass, and the draft phase.
   * nvidia-smi samples clocks and throttle reasons during the timed region.
 
 `--impl reference` times the fp64 CPU oracle on the same workload (the only
@@ -38,19 +43,25 @@ if ROOT not in sys.path:
 
 METRIC = "µs per verify+select+sparse-draft iteration"
 UNIT = "us/iteration"
+DEFAULT_WORKLOAD = "loop32"
+SECONDARY = "llama8b,long70b,batched"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--secondary", default=None,
+                    help="comma-separated one-layer workloads measured per phase beside the headline "
+                         f"(default: {SECONDARY} when the headline is {DEFAULT_WORKLOAD}; 'none' to skip)")
+    ap.add_argument("--secondary-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=None)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ distributed
@@ -145,7 +156,8 @@ def workload_desc(w) -> str:
 
 
 def algorithmic_bytes(w, lengths) -> dict:
-    """KV bytes one iteration must read: the prefix once for verify, k + s + 1 slots per draft step."""
+    """KV bytes one layer's iteration must read: the prefix once for verify, k + s + 1
+    slots per draft step (the selection, then the draft tokens so far)."""
     per_tok = w.Hkv * w.d * 2 * 2
     verify = int(sum(lengths)) * per_tok
     draft = 0
@@ -165,7 +177,8 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-VERIFY_SOURCES = ("verify_attn.cu", "attn_frag.cuh", "vg_common.cuh", "vg_internal.h")
+VERIFY_SOURCES = ("verify_attn.cu", "vg_common.cuh", "vg_internal.h")
+DRAFT_SOURCES = ("sparse_draft.cu", "attn_frag.cuh", "vg_common.cuh", "vg_internal.h")
 
 
 def strip_c_comments(src: str) -> str:
@@ -192,34 +205,37 @@ def strip_c_comments(src: str) -> str:
     return "\n".join(ln.rstrip() for ln in "".join(out).split("\n") if ln.strip())
 
 
-def verify_source_sha() -> str:
-    """sha256 over the code (comments left out) the verify kernel is compiled from."""
+def source_sha(files=VERIFY_SOURCES) -> str:
+    """sha256 over the code (comments left out) a kernel is compiled from."""
     h = hashlib.sha256()
-    for f in VERIFY_SOURCES:
+    for f in files:
         src = open(os.path.join(ROOT, "self_speculative_sparse_gb300", "csrc", f), encoding="utf-8").read()
         h.update(strip_c_comments(src).encode())
     return h.hexdigest()
 
 
-def profiled_traffic(workload: str):
-    """Per-launch DRAM bytes of the verify kernel from the committed ncu summary, if it
-    was taken on the current sources (the summary records their sha256)."""
-    prof = os.path.join(ROOT, "profiles", f"verify_attn_{workload}.md")
+def verify_source_sha() -> str:
+    return source_sha(VERIFY_SOURCES)
+
+
+def profiled_traffic(kernel: str, workload: str, files) -> int | None:
+    """Per-launch DRAM bytes of a kernel from its committed ncu summary
+    (profiles/<kernel>_<workload>.md), if it was taken on the current sources (the
+    summary records their sha256)."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(prof):
         return None
-    sha = verify_source_sha()
     vals = {}
     for line in open(prof):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256") != sha:
+    if vals.get("source_sha256") != source_sha(files):
         return None
     try:
         return int(float(vals["dram_bytes_per_launch"]))
     except (KeyError, ValueError):
         return None
-
 
 
 def pack_views(state, names, copy_values: bool):
@@ -241,10 +257,18 @@ def pack_views(state, names, copy_values: bool):
         setattr(state, nm, v)
     return buf
 
+
+def overlap_fraction(a, b, k) -> float:
+    """|A ∩ B| / k of two selections (a reported statistic of the bench)."""
+    import numpy as np
+    if k <= 0:
+        return 1.0
+    return len(np.intersect1d(a, b)) / float(k)
+
+
 # ------------------------------------------------------------------ CPU oracle timing
 def oracle_iteration_time(w, pool, budget_s: float, max_reps: int = 1000):
     """Time the fp64 oracle on whole iterations of sequence 0 of the workload."""
-    import numpy as np
     import oracle
     from oracle import widen_bf16
     o, n = int(pool["seq_offset"][0]), int(pool["prefix_len"][0])
@@ -276,14 +300,21 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
+def oracle_scale(w, lengths, n0: int) -> float:
+    """Factor from one oracle iteration of sequence 0 to the whole workload: prefix tokens
+    (the verification dominates the oracle's work) and layers."""
+    return w.layers * float(sum(int(n) for n in lengths)) / n0
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
     import synth
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
+    lengths = w.lengths()
     if w.layers > 1 or w.B > 1:
-        w_sample = synth.scaled(w, B=1, layers=1, n=int(w.lengths()[0]), ragged=None)
+        w_sample = synth.scaled(w, B=1, layers=1, n=int(lengths[0]), ragged=None)
     else:
         w_sample = w
     pool = w_sample.layer_pool(0)
@@ -292,11 +323,11 @@ def run_reference(args, rank, world):
     times = []
     for _ in range(args.steps):
         times += oracle_iteration_time(w_sample, pool, 0.0, max_reps=1)
-    # one oracle iteration covers one sequence of one layer; scale to the workload
-    scale = w.B * w.layers if (w.layers > 1 or w.B > 1) else 1
+    n0 = int(pool["prefix_len"][0])
+    scale = oracle_scale(w, lengths, n0)
     per_iter_us = statistics.mean(times) * 1e6 * scale
-    sample = (f"{args.steps} oracle iterations of sequence 0 (n={int(pool['prefix_len'][0])}), "
-              f"scaled x{scale} to the workload" if scale > 1 else
+    sample = (f"{args.steps} oracle iterations of sequence 0 (n={n0}), scaled x{scale:.2f} to the workload's "
+              f"prefix tokens and layers" if scale != 1.0 else
               f"{args.steps} full oracle iterations of the workload")
     line = {
         "impl": "reference", "metric": METRIC, "value": per_iter_us, "unit": UNIT, "n_gpus": args.gpus,
@@ -311,103 +342,218 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ our arm
+class Setup:
+    """A workload resident on the GPU, with the step and per-phase call sequences."""
+
+    def __init__(self, w, local: int):
+        import torch
+        from self_speculative_sparse_gb300.runtime import LayerState
+        self.w = w
+        self.multi = w.layers > 1
+        dev = f"cuda:{local}"
+        self.pool = w.layer_pool(0)
+        self.lengths = self.pool["prefix_len"]
+        self.layer_bytes = int(self.pool["K"].nbytes + self.pool["V"].nbytes)
+        self.l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        if self.multi:
+            # every layer resident (each far larger than L2): the model's own order streams them
+            self.ncopy = w.layers
+            self.states = [LayerState(w, self.pool, device=dev)]
+            for layer in range(1, w.layers):
+                self.states.append(LayerState(w, w.layer_pool(layer), device=dev))
+        else:
+            # rotating copies of the one layer, so every kernel reads its cache cold
+            self.ncopy = max(3, -(-4 * self.l2 // self.layer_bytes) + 1)
+            self.states = [LayerState(w, self.pool, device=dev) for _ in range(self.ncopy)]
+        self.stream = torch.cuda.current_stream()
+        self.tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device=dev) for s in range(w.gamma)]
+        self.half = self.ncopy // 2
+        # per layer: the prefix once for verify, the selection + draft tokens per draft step
+        self.nbytes = {k: v * w.layers for k, v in algorithmic_bytes(w, self.lengths).items()}
+        # every copy gets one full iteration first, so each has its own selection
+        for st in self.states:
+            st.iteration(stream=self.stream, select_extra=False)
+        torch.cuda.synchronize()
+        self.check("set-up")
+
+    def check(self, when: str) -> None:
+        bad = [(i, st.check_status()) for i, st in enumerate(self.states) if st.check_status() != 0]
+        if bad:
+            raise RuntimeError(f"device status at {when} (copy, code): {bad}")
+
+    def draft_phase(self, st) -> None:
+        for s in range(self.w.gamma):
+            st.draft_step(s, self.tl[s])
+
+    def step(self, i: int) -> None:
+        if self.multi:  # the model's order: verify every layer, select, then each draft step over the layers
+            for st in self.states:
+                st.verify()
+                st.select()
+            for s in range(self.w.gamma):
+                for st in self.states:
+                    st.draft_step(s, self.tl[s])
+            return
+        # one layer: verify + select on copy i, the draft phase on copy i + ncopy/2
+        a, b = self.states[i % self.ncopy], self.states[(i + self.half) % self.ncopy]
+        a.verify()
+        a.select()
+        self.draft_phase(b)
+
+    def phase_calls(self, i: int, which: str) -> None:
+        """The calls of step(i) for one phase only: 'v' verify, 's' select, 'd' draft."""
+        if self.multi:
+            for st in self.states:
+                if which == "v":
+                    st.verify()
+                elif which == "s":
+                    st.select()
+            if which == "d":
+                for s in range(self.w.gamma):
+                    for st in self.states:
+                        st.draft_step(s, self.tl[s])
+            return
+        if which == "v":
+            self.states[i % self.ncopy].verify()
+        elif which == "s":
+            self.states[i % self.ncopy].select()
+        else:
+            self.draft_phase(self.states[(i + self.half) % self.ncopy])
+
+    def verify_masked(self, i: int, m0: int) -> None:
+        """The verify call of step(i) with one score mask (or none)."""
+        from self_speculative_sparse_gb300 import binding as vb
+        sts = self.states if self.multi else [self.states[i % self.ncopy]]
+        for st in sts:
+            vb.vg_verify_attn(st.dims, st.cache, st.q_verify, st.k_new, st.v_new, st.prefix_len, m0, 0,
+                              st.scores0 if m0 else None, None, st.score_stride, st.out_verify, st.ws,
+                              dev_status=st.status)
+
+
+def capture(fn):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        fn()
+    return g
+
+
+def time_graph_us(g, stream, reps: int) -> float:
+    """Mean µs per rep of a graph holding `reps` reps: launched once untimed (its upload),
+    then once between two events on the launching stream."""
+    import torch
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def phase_times(S: Setup, first: int, steps: int) -> dict:
+    """Per-phase µs of one step (sums over the layers of a multi-layer workload)."""
+    t = {}
+    for which, nm in (("v", "verify_call"), ("s", "select"), ("d", "draft_gamma_steps")):
+        g = capture(lambda which=which: [S.phase_calls(first + i, which) for i in range(steps)])
+        t[nm] = time_graph_us(g, S.stream, steps)
+        del g
+    t["per_draft_step"] = t["draft_gamma_steps"] / max(1, S.w.gamma)
+    return t
+
+
+def score_cost(S: Setup, first: int, steps: int) -> dict:
+    """The verify call without scores, with the Collect-2-Query rows and with all rows."""
+    w = S.w
+    R = w.gamma + 1
+    variants = {"no_scores": 0, "collect2": (1 | (1 << w.gamma)), "all_rows": (1 << R) - 1}
+    out = {}
+    for nm, m0 in variants.items():
+        g = capture(lambda m0=m0: [S.verify_masked(first + i, m0) for i in range(steps)])
+        out[nm] = time_graph_us(g, S.stream, steps)
+        del g
+    base = out["no_scores"]
+    for nm in ("collect2", "all_rows"):
+        out[nm + "_overhead_pct"] = 100.0 * (out[nm] - base) / base
+    return out
+
+
+def fractions(S: Setup, ph: dict, peak: float) -> dict:
+    """Three HBM fractions, each recomputable from phases_us and the algorithmic bytes:
+    the verify call alone, the fused verify+select pass, and the draft phase."""
+    vb_, db_ = S.nbytes["verify"], S.nbytes["draft"]
+    def f(nbytes, us):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"achieved_gbs": gbs, "frac": gbs / peak, "bytes": nbytes, "us": us}
+    return {"verify_call": f(vb_, ph["verify_call"]),
+            "verify_select": f(vb_, ph["verify_call"] + ph["select"]),
+            "draft_phase": f(db_, ph["draft_gamma_steps"])}
+
+
+def selection_stats(S: Setup, score_us: dict, ph: dict, iter_us: float) -> dict:
+    """Selection overhead (score emission + top-k) as a share of the iteration, and the
+    overlap of the Collect-2-Query selection with the all-rows selection where both run."""
+    import torch
+    w = S.w
+    mask_key = "collect2" if w.select_rows == "c2" else "all_rows"
+    emit = score_us[mask_key] - score_us["no_scores"]
+    out = {"score_emission_us": emit, "select_us": ph["select"],
+           "selection_overhead_pct": 100.0 * (emit + ph["select"]) / iter_us,
+           "note": "(verify with the selection mask - verify without scores + top-k) / iteration"}
+    if w.extra_rows:
+        ov = []
+        for st in S.states[:1]:
+            st.iteration(stream=S.stream, select_extra=True)
+            torch.cuda.synchronize()
+            idx, idx1 = st.idx.cpu().numpy(), st.idx1.cpu().numpy()
+            cnt = st.count.cpu().numpy()
+            for b in range(w.B):
+                c = int(cnt[b])
+                ov.append(overlap_fraction(idx[b, :c], idx1[b, :c], c))
+        out["overlap_" + w.select_rows + "_vs_" + w.extra_rows] = {
+            "mean": float(sum(ov) / len(ov)), "min": float(min(ov)), "sequences": len(ov)}
+    return out
+
+
+def secondary_line(name: str, local: int, steps: int, peak: float) -> dict:
+    import synth
+    import torch
+    w = synth.WORKLOADS[name]
+    S = Setup(w, local)
+    ph = phase_times(S, 0, steps)
+    sc = score_cost(S, 0, steps)
+    g_run = capture(lambda: [S.step(i) for i in range(steps)])
+    it_us = time_graph_us(g_run, S.stream, steps)
+    del g_run
+    S.check("secondary " + name)
+    out = {"workload": workload_desc(w), "us_per_iteration": it_us, "phases_us": ph,
+           "fractions_of_hbm": fractions(S, ph, peak), "verify_call_by_score_rows_us": sc,
+           "selection": selection_stats(S, sc, ph, it_us)}
+    del S
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, local, world):
-    import numpy as np
     import torch
     import synth
     from self_speculative_sparse_gb300 import build as vbuild
-    from self_speculative_sparse_gb300 import binding as vb
-    from self_speculative_sparse_gb300.runtime import LayerState
 
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
     vbuild.build()
     w = synth.WORKLOADS[args.workload]
-    multi = w.layers > 1
-    pool = w.layer_pool(0)
-    lengths = pool["prefix_len"]
-    nbytes = {k: v * w.layers for k, v in algorithmic_bytes(w, lengths).items()}
-    layer_bytes = int(pool["K"].nbytes + pool["V"].nbytes)
-    l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    if multi:
-        # every layer resident (each far larger than L2): the model's own order streams them
-        ncopy = w.layers
-        states = [LayerState(w, pool, device=f"cuda:{local}")]
-        for layer in range(1, w.layers):
-            states.append(LayerState(w, w.layer_pool(layer), device=f"cuda:{local}"))
-    else:
-        # rotating copies of the one layer, so every kernel reads its cache cold
-        ncopy = max(3, -(-4 * l2 // layer_bytes) + 1)
-        states = [LayerState(w, pool, device=f"cuda:{local}") for _ in range(ncopy)]
-    stream = torch.cuda.current_stream()
-    tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device=f"cuda:{local}") for s in range(w.gamma)]
-
-    def draft_phase(st):  # on the current stream (the capture stream inside a graph capture)
-        for s in range(w.gamma):
-            st.draft_step(s, tl[s])
-
-    # every copy gets one full iteration first, so each has its own selection
-    for st in states:
-        st.iteration(stream=stream, select_extra=False)
-    torch.cuda.synchronize()
-    for st in states:
-        if st.check_status() != 0:
-            raise RuntimeError(f"device status {st.check_status()}")
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="thread_local"):
-            fn()
-        return g
-
-    half = ncopy // 2
-
-    def step(i):
-        if multi:  # the model's order: verify every layer, select, then each draft step over the layers
-            for st in states:
-                st.verify()
-                st.select()
-            for s in range(w.gamma):
-                for st in states:
-                    st.draft_step(s, tl[s])
-            return
-        # one layer: verify + select on copy i, the draft phase on copy i + ncopy/2
-        a, b = states[i % ncopy], states[(i + half) % ncopy]
-        a.verify()
-        a.select()
-        draft_phase(b)
-
-    def phase_calls(i, which):  # the same calls as step(i), one phase only
-        if multi:
-            for st in states:
-                if which == "v":
-                    st.verify()
-                elif which == "s":
-                    st.select()
-            if which == "d":
-                for s in range(w.gamma):
-                    for st in states:
-                        st.draft_step(s, tl[s])
-            return
-        if which == "v":
-            states[i % ncopy].verify()
-        elif which == "s":
-            states[i % ncopy].select()
-        else:
-            draft_phase(states[(i + half) % ncopy])
+    S = Setup(w, local)
+    stream, multi, ncopy = S.stream, S.multi, S.ncopy
 
     # One graph per timed run (a serving loop replays captured decode steps, so the
     # host's launch cost stays off the GPU timeline); warm-up steps in a graph of their own.
-    g_warm = capture(lambda: [step(i) for i in range(args.warmup)])
-    g_run = capture(lambda: [step(args.warmup + i) for i in range(args.steps)])
-    # per-phase breakdown: the same calls, one phase at a time, K back to back
-    g_v = capture(lambda: [phase_calls(args.warmup + i, "v") for i in range(args.steps)])
-    g_s = capture(lambda: [phase_calls(args.warmup + i, "s") for i in range(args.steps)])
-    g_d = capture(lambda: [phase_calls(args.warmup + i, "d") for i in range(args.steps)])
+    g_warm = capture(lambda: [S.step(i) for i in range(args.warmup)])
+    g_run = capture(lambda: [S.step(args.warmup + i) for i in range(args.steps)])
     torch.cuda.synchronize()
-    for g in (g_run, g_v, g_s, g_d):  # each graph's first launch (it uploads the graph), untimed
-        g.replay()
+    g_run.replay()  # the graph's first launch (it uploads the graph), untimed
     torch.cuda.synchronize()
 
     # ---- headline: K steps between two events, right after the W warm-up steps (the
@@ -426,30 +572,20 @@ def run_ours(args, rank, local, world):
     torch.cuda.synchronize()
     barrier(world)
     ms_total = e0.elapsed_time(e1)
-    # ---- per-phase events
-    ph = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    ph[0].record(stream)
-    g_v.replay()
-    ph[1].record(stream)
-    g_s.replay()
-    ph[2].record(stream)
-    g_d.replay()
-    ph[3].record(stream)
-    torch.cuda.synchronize()
     clk = clocks.stop()
+    del g_warm, g_run
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
-    t_verify = ph[0].elapsed_time(ph[1]) * 1e3 / args.steps
-    t_select = ph[1].elapsed_time(ph[2]) * 1e3 / args.steps
-    t_draft = ph[2].elapsed_time(ph[3]) * 1e3 / args.steps
+    ph = phase_times(S, args.warmup, args.steps)
+
     # ---- K steps launched eagerly (no graph): one vg_iteration call per step (the
     # model's per-layer calls for the multi-layer workload); the mean from two events
     # around them, the spread from a second pass with an event between steps
     def eager_step(i):
         if multi:
-            step(i)
+            S.step(i)
         else:
-            states[i % ncopy].iteration(stream=stream, select_extra=False)
+            S.states[i % ncopy].iteration(stream=stream, select_extra=False)
 
     torch.cuda.synchronize()
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -469,65 +605,34 @@ def run_ours(args, rank, local, world):
 
     def pct(v, q):
         return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+
     # ---- secondary: the draft phase with its gathered entries warm in L2 (K draft
     # phases on one cache copy), where the headline reads every step cold
     draft_warm = None
     if not multi:
-        g_dw = capture(lambda: [draft_phase(states[0]) for _ in range(args.steps)])
-        g_dw.replay()
-        torch.cuda.synchronize()
-        ew = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ew[0].record(stream)
-        g_dw.replay()
-        ew[1].record(stream)
-        torch.cuda.synchronize()
-        draft_warm = ew[0].elapsed_time(ew[1]) * 1e3 / args.steps / max(1, w.gamma)
-    # ---- cost of the fused logit aggregation: the verify call with no scores, with the
-    # Collect-2-Query rows and with all rows (same rotation, K back-to-back calls)
-    R = w.gamma + 1
-    variants = {"no_scores": 0, "collect2": (1 | (1 << w.gamma)), "all_rows": (1 << R) - 1}
+        g_dw = capture(lambda: [S.draft_phase(S.states[0]) for _ in range(args.steps)])
+        draft_warm = time_graph_us(g_dw, stream, args.steps) / max(1, w.gamma)
+        del g_dw
+    sc = score_cost(S, args.warmup, args.steps)
+    S.check("timed runs")
 
-    def verify_masked(st, m0):
-        vb.vg_verify_attn(st.dims, st.cache, st.q_verify, st.k_new, st.v_new, st.prefix_len, m0, 0,
-                          st.scores0 if m0 else None, None, st.score_stride, st.out_verify, st.ws,
-                          dev_status=st.status)
-
-    score_cost = {}
-    if not multi:
-        gv = {nm: capture(lambda m0=m0: [verify_masked(states[(args.warmup + i) % ncopy], m0)
-                                         for i in range(args.steps)]) for nm, m0 in variants.items()}
-        for nm, g in gv.items():
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            ev[0].record(stream)
-            g.replay()
-            ev[1].record(stream)
-            torch.cuda.synchronize()
-            score_cost[nm] = ev[0].elapsed_time(ev[1]) * 1e3 / args.steps
-        base = score_cost["no_scores"]
-        for nm in ("collect2", "all_rows"):
-            score_cost[nm + "_overhead_pct"] = 100.0 * (score_cost[nm] - base) / base
-    bad = [(i, st.check_status()) for i, st in enumerate(states) if st.check_status() != 0]
-    if bad:
-        raise RuntimeError(f"device status (copy, code): {bad}")
-
-    # ---- end to end through the public C ABI (vg_iteration) with host buffers.  A
-    # step's inputs sit in one pinned host buffer and one device buffer (the tensors
-    # the call reads are views into it), so one copy brings them in; the outputs the
-    # same way, one copy out.
+    # ---- end to end through the public C ABI with host buffers.  A step's inputs sit
+    # in one pinned host buffer and one device buffer (the tensors the call reads are
+    # views into it), so one copy brings them in; the outputs the same way, one copy out.
     e2e_steps = args.e2e_steps or args.steps
     in_names = ("q_verify", "k_new", "v_new", "q_draft", "k_draft", "v_draft")
     out_names = ("out_verify", "idx", "count", "out_draft")
-    e2e_states = states if multi else states[:ncopy]
     staged = []
-    for a in e2e_states:
+    for a in S.states:
         dev_in = pack_views(a, in_names, copy_values=True)
         dev_out = pack_views(a, out_names, copy_values=False)
         host_in = torch.empty_like(dev_in, device="cpu").pin_memory()
         host_in.copy_(dev_in)
         host_out = torch.empty_like(dev_out, device="cpu").pin_memory()
         staged.append((a, dev_in, host_in, dev_out, host_out))
-    bi = sum(getattr(states[0], nm).numel() * getattr(states[0], nm).element_size() for nm in in_names)
-    bo = sum(getattr(states[0], nm).numel() * getattr(states[0], nm).element_size() for nm in out_names)
+    st0 = S.states[0]
+    bi = sum(getattr(st0, nm).numel() * getattr(st0, nm).element_size() for nm in in_names)
+    bo = sum(getattr(st0, nm).numel() * getattr(st0, nm).element_size() for nm in out_names)
     bi, bo = bi * (w.layers if multi else 1), bo * (w.layers if multi else 1)
 
     # Copies run on streams of their own, as a serving loop overlaps them: a step's inputs
@@ -575,28 +680,28 @@ def run_ours(args, rank, local, world):
     barrier(world)
     for pl in plans:
         pl.close()
-    bad = [(i, st.check_status()) for i, st in enumerate(e2e_states) if st.check_status() != 0]
-    if bad:
-        raise RuntimeError(f"device status after the end-to-end steps (copy, code): {bad}")
+    S.check("end-to-end steps")
 
     us_iter = ms_step * 1e3 / world  # whole-job: iterations of all ranks per unit time
     peaks = measured_peaks()
-    verify_gbs = nbytes["verify"] / (t_verify * 1e-6) / 1e9
-    kv_gbs = (nbytes["verify"] + nbytes["draft"]) / (ms_step * 1e-3) / 1e9
-    launches_per_step = (2 + 1 + 2 * w.gamma) * (w.layers if multi else 1)
+    fr = fractions(S, ph, peaks["hbm_gbs"])
+    kv_gbs = (S.nbytes["verify"] + S.nbytes["draft"]) / (ms_step * 1e-3) / 1e9
+    launches_per_step = S.states[0].launches_per_iteration() * (w.layers if multi else 1)
+    verify_launches = w.layers if multi else 1
     line = {
         "metric": METRIC, "value": us_iter, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w),
-                   "l2": (f"{w.layers} resident layers of {layer_bytes / 1e6:.0f} MB each (L2 {l2 / 1e6:.0f} MB): "
-                          f"verify over every layer, then each draft step over every layer" if multi else
-                          f"{ncopy} rotating cache copies of {layer_bytes / 1e6:.0f} MB (> 4x L2 of "
-                          f"{l2 / 1e6:.0f} MB); draft on a different copy than the verify before it"),
+                   "l2": (f"{w.layers} resident layers of {S.layer_bytes / 1e6:.0f} MB each (L2 "
+                          f"{S.l2 / 1e6:.0f} MB): verify over every layer, then each draft step over every layer"
+                          if multi else
+                          f"{ncopy} rotating cache copies of {S.layer_bytes / 1e6:.0f} MB (> 4x L2 of "
+                          f"{S.l2 / 1e6:.0f} MB); draft on a different copy than the verify before it"),
                    "timing": ("K steps replayed as one CUDA graph, CUDA events around it; the graph is launched "
                               "once untimed first (its upload), the W warm-up steps run just before it"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "kv_bytes_per_iteration": nbytes["verify"] + nbytes["draft"],
+        "kv_bytes_per_iteration": S.nbytes["verify"] + S.nbytes["draft"],
         "kv_gbs": kv_gbs, "kv_pct_of_hbm": 100.0 * kv_gbs / peaks["hbm_gbs"],
         "eager_launches_us": {"mean": eager_mean, "p10": pct(eager_steps, 0.1), "p50": pct(eager_steps, 0.5),
                               "p90": pct(eager_steps, 0.9),
@@ -604,15 +709,19 @@ def run_ours(args, rank, local, world):
                                       "by one; the multi-layer workload: its per-layer calls in the model's "
                                       "order); percentiles over steps timed with an event between steps"},
         "draft_step_l2_warm_us": draft_warm,
-        "phases_us": {"verify_call": t_verify, "select": t_select, "draft_gamma_steps": t_draft,
-                      "per_draft_step": t_draft / max(1, w.gamma)},
+        "phases_us": ph,
         "phases_note": "sums over the layers of one step" if multi else "one layer",
-        "verify_call_by_score_rows_us": score_cost,
-        "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine)", "bound": "hbm",
-                     "achieved": verify_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": verify_gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": profiled_traffic(w.name),
-                     "algorithmic_bytes": nbytes["verify"]},
+        "fractions_of_hbm": fr,
+        "verify_call_by_score_rows_us": sc,
+        "selection": selection_stats(S, sc, ph, ms_step * 1e3),
+        "roofline": {"kernel": "vg_verify_attn (verify_kernel + combine), the largest share of the step",
+                     "bound": "hbm", "achieved": fr["verify_call"]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": fr["verify_call"]["frac"], "peak_source": peaks["source"],
+                     "traffic": profiled_traffic("verify_attn", w.name, VERIFY_SOURCES),
+                     "algorithmic_bytes_per_launch": S.nbytes["verify"] / verify_launches,
+                     "launch_us": ph["verify_call"] / verify_launches,
+                     "parts": {k: {"bound": "hbm", "achieved": v["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": v["frac"]} for k, v in fr.items()}},
         "e2e": {"value": e2e_s / e2e_steps * 1e6 / world, "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo,
                 "api": "vg_iteration_plan_launch (each buffer set's iteration captured once at set-up)",
@@ -621,12 +730,20 @@ def run_ours(args, rank, local, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
+    pool, lengths = S.pool, S.lengths
+    del staged, plans, S
+    torch.cuda.empty_cache()
+
+    names = args.secondary if args.secondary is not None else (SECONDARY if args.workload == DEFAULT_WORKLOAD
+                                                               else "none")
+    if rank == 0 and names != "none":
+        line["workloads"] = {}
+        for nm in [x for x in names.split(",") if x and x != args.workload]:
+            line["workloads"][nm] = secondary_line(nm, local, args.secondary_steps, peaks["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times = oracle_iteration_time(w, pool, args.cpu_seconds)
-        # sequence 0 of layer 0 is timed; the whole workload's time is scaled by prefix
-        # tokens (the verification dominates the oracle's work) and by layers
         n0 = int(lengths[0])
-        scale = w.layers * float(sum(int(n) for n in lengths)) / n0
+        scale = oracle_scale(w, lengths, n0)
         line["cpu_baseline"] = {"value": statistics.mean(times) * 1e6 * scale, "unit": UNIT, "cores": cpu_threads(),
                                 "kind": "oracle",
                                 "sample": f"{len(times)} fp64 oracle iterations of sequence 0 (n={n0}; verify, "

@@ -137,6 +137,11 @@ def make_cache(K, V, seq_offset, capacity_slots: int | None = None) -> vg_kv_cac
     return vg_kv_cache(ptr(K), ptr(V), ptr(seq_offset), cap)
 
 
+def draft_launches(dims: vg_dims) -> int:
+    """Kernels one vg_sparse_draft_attn call enqueues (the gather kernel and its merge)."""
+    return 2
+
+
 def vg_workspace_size(dims: vg_dims, k: int) -> int:
     n = load().vg_workspace_size(ctypes.byref(dims), k)
     if n == 0:

@@ -106,6 +106,11 @@ class LayerState:
                                 self.count, self.k, self.prefix_len, tail_len, self.out_draft[s], self.ws,
                                 dev_status=self.status, stream=stream)
 
+    def launches_per_iteration(self, select_extra: bool = False) -> int:
+        """Kernels one vg_iteration enqueues: the verify kernel and its combine, one
+        selection (two with select_extra), and the draft kernels of each draft step."""
+        return 2 + (2 if select_extra and self.mask1 else 1) + self.gamma * vb.draft_launches(self.dims)
+
     def check_status(self) -> int:
         return int(self.status.item())
 
