@@ -686,7 +686,7 @@ def run_ours(args, rank, local, world):
     peaks = measured_peaks()
     fr = fractions(S, ph, peaks["hbm_gbs"])
     kv_gbs = (S.nbytes["verify"] + S.nbytes["draft"]) / (ms_step * 1e-3) / 1e9
-    launches_per_step = S.states[0].launches_per_iteration() * (w.layers if multi else 1)
+    launches_per_step = S.states[0].launches_per_iteration(tail_from_device=True) * (w.layers if multi else 1)
     verify_launches = w.layers if multi else 1
     line = {
         "metric": METRIC, "value": us_iter, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -149,18 +149,30 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
  * If k_new / v_new (bf16 [B][H_kv][d]) are non-NULL they are the current draft
  * token's key and value: they are appended at slot tail_start[b] + tail_len[b] - 1
  * (tail_len[b] >= 1 is then required) and attended from the inputs directly.
- * tail_len[b] <= 64; a longer tail is reported as VG_ERR_DEVICE_BOUNDS.
+ * tail_len[b] <= 16 (a draft phase appends at most gamma + 1 <= 16 tokens); a longer
+ * tail is reported as VG_ERR_DEVICE_BOUNDS.  k_stride <= 2^24.
  * Selected positions must be < tail_start[b]; entries outside [0, tail_start[b]) are
  * skipped and reported as VG_ERR_DEVICE_BOUNDS.
  *
  *   q      bf16 [B][H_q][d]             idx  int32 [B][k_stride], count int32 [B] (<= k_stride)
  *   tail_start, tail_len  device int32 [B]   out  bf16 [B][H_q][d]
+ *   flags  0, or VG_DRAFT_SELECTION_SETTLED (below); other bits are VG_ERR_INVALID_ARG.
  */
+/* The caller vouches that idx, count, seq_offset, tail_start, tail_len and the cache
+ * entries at the selected positions were all written before the kernel that precedes
+ * this call in the stream began.  That holds for every draft step of a phase after the
+ * first: the selection is made once per verification and the steps in between only
+ * append draft tokens (Vegas §2 step 3).  The call then starts gathering the selected
+ * entries before its dependency on that preceding kernel resolves, overlapping the
+ * end of the previous step; the draft-token tail still waits for it.  Results are
+ * unspecified if the promise does not hold. */
+#define VG_DRAFT_SELECTION_SETTLED 1u
+
 vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q,
                                const void* k_new, const void* v_new, const int32_t* idx,
                                const int32_t* count, int32_t k_stride, const int32_t* tail_start,
-                               const int32_t* tail_len, void* out, void* ws, size_t ws_bytes,
-                               int32_t* dev_status, void* stream);
+                               const int32_t* tail_len, uint32_t flags, void* out, void* ws,
+                               size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Inputs of one iteration (host struct of device pointers). */
 typedef struct vg_iter_inputs {
@@ -238,8 +250,8 @@ vg_status vg_iteration_plan_destroy(vg_iteration_plan* plan);
  * device memory, for example a host that must not call cudaMalloc during decoding
  * (the call can synchronise the device and stall other streams) or that has no
  * workspace to offer.  Same computation, arguments and results as
- * vg_sparse_draft_attn; the scratch space comes from an 8 MiB area inside the
- * library that every GPU using the library keeps until the process exits.
+ * vg_sparse_draft_attn with flags 0; the scratch space comes from an 8 MiB area
+ * inside the library that every GPU using the library keeps until the process exits.
  *   - It allocates and frees nothing.
  *   - Dimensions whose draft scratch exceeds 8 MiB are rejected with
  *     VG_ERR_WORKSPACE (for 152 SMs: about H_q * (152 + B) * (d + 2) * 4 bytes).
@@ -259,6 +271,15 @@ vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* c
 /* Bytes of workspace any call above needs for these dimensions on the current
  * device (0 on invalid dims or no device; see vg_last_error()). */
 size_t vg_workspace_size(const vg_dims* dims, int32_t k);
+
+/* Kernels one vg_sparse_draft_attn call with these dimensions enqueues on the current
+ * device: 1 when every sequence's entries fall to a single CTA of the step's grid
+ * (that CTA finishes the sequence), else 2 (a second kernel merges the partials).  tail_len_max is the
+ * longest tail the call may attend, 0 for the bound of a device tail_len array (16).
+ * Returns 0 on invalid arguments or when no device is present (see vg_last_error()).
+ * vg_iteration enqueues 3 (verify, its merge, the selection; 4 with a second
+ * selection) plus gamma times this number for tail_len_max = 1 .. gamma. */
+int32_t vg_sparse_draft_launches(const vg_dims* dims, int32_t k_stride, int32_t tail_len_max);
 
 /* Human-readable description of the last error on this host thread ("" if none). */
 const char* vg_last_error(void);

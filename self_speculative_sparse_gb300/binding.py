@@ -24,8 +24,8 @@ VG_ERR_DEVICE_BOUNDS = -6
 
 ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_sparse_draft_attn", "vg_iteration",
                 "vg_iteration_plan_create", "vg_iteration_plan_launch", "vg_iteration_plan_destroy",
-                "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_last_error", "vg_version",
-                "vg_selftest_lost_wait")
+                "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_sparse_draft_launches",
+                "vg_last_error", "vg_version", "vg_selftest_lost_wait")
 
 
 class VgError(RuntimeError):
@@ -76,7 +76,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_topk_select.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
     L.vg_topk_select.restype = i32
     L.vg_sparse_draft_attn.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), vp, vp, vp, vp, vp,
-                                       i32, vp, vp, vp, vp, sz, vp, vp]
+                                       i32, vp, vp, u32, vp, vp, sz, vp, vp]
     L.vg_sparse_draft_attn.restype = i32
     L.vg_sparse_draft_attn_noalloc.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), vp, vp, vp,
                                                vp, vp, i32, vp, vp, vp, vp, vp]
@@ -94,6 +94,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_iteration_plan_destroy.restype = i32
     L.vg_workspace_size.argtypes = [ctypes.POINTER(vg_dims), i32]
     L.vg_workspace_size.restype = sz
+    L.vg_sparse_draft_launches.argtypes = [ctypes.POINTER(vg_dims), i32, i32]
+    L.vg_sparse_draft_launches.restype = i32
     L.vg_last_error.argtypes = []
     L.vg_last_error.restype = ctypes.c_char_p
     L.vg_version.argtypes = []
@@ -137,9 +139,12 @@ def make_cache(K, V, seq_offset, capacity_slots: int | None = None) -> vg_kv_cac
     return vg_kv_cache(ptr(K), ptr(V), ptr(seq_offset), cap)
 
 
-def draft_launches(dims: vg_dims) -> int:
-    """Kernels one vg_sparse_draft_attn call enqueues (the gather kernel and its merge)."""
-    return 2
+def vg_sparse_draft_launches(dims: vg_dims, k_stride: int, tail_len_max: int = 0) -> int:
+    """Kernels one vg_sparse_draft_attn call enqueues (1 or 2) for these dimensions."""
+    n = load().vg_sparse_draft_launches(ctypes.byref(dims), k_stride, tail_len_max)
+    if n == 0:
+        raise VgError(VG_ERR_INVALID_ARG, load().vg_last_error().decode())
+    return n
 
 
 def vg_workspace_size(dims: vg_dims, k: int) -> int:
@@ -163,12 +168,15 @@ def vg_topk_select(scores, score_stride, len_, B, max_len, k, idx, count, ws=Non
                                  ptr(ws), ws_bytes, ptr(dev_status), _stream(stream)))
 
 
+VG_DRAFT_SELECTION_SETTLED = 1
+
+
 def vg_sparse_draft_attn(dims, cache, q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, out, ws,
-                         ws_bytes=None, dev_status=None, stream=None) -> None:
+                         ws_bytes=None, dev_status=None, stream=None, flags: int = 0) -> None:
     wsb = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
     _check(load().vg_sparse_draft_attn(ctypes.byref(dims), ctypes.byref(cache), ptr(q), ptr(k_new), ptr(v_new),
-                                       ptr(idx), ptr(count), k_stride, ptr(tail_start), ptr(tail_len), ptr(out),
-                                       ptr(ws), wsb, ptr(dev_status), _stream(stream)))
+                                       ptr(idx), ptr(count), k_stride, ptr(tail_start), ptr(tail_len), flags,
+                                       ptr(out), ptr(ws), wsb, ptr(dev_status), _stream(stream)))
 
 
 def vg_iteration(dims, cache, inputs: vg_iter_inputs, k, row_mask0, row_mask1, outputs: vg_iter_outputs, ws,

@@ -69,6 +69,10 @@ __device__ __forceinline__ void qk16(const uint32_t (&qf)[D / 16][4], KAddr kadd
 
 // Online-softmax update with 16 logits per row already in log2 units (masked
 // keys at -inf), then O += P V.  vaddr(r, c16) as kaddr, for the value rows.
+// P goes to the tensor cores as a bf16 high part plus a bf16 low part, P - bf16(P),
+// each multiplied with the same value fragments, so the weights carry about 16 bits
+// (relative error near 2^-17) and agree with the fp32 row sum l: rounding P to bf16
+// alone would move a row whose weight sits on a few keys by up to 2^-9 of its values.
 template <int D, typename VAddr>
 __device__ __forceinline__ void softmax_pv16(RowState<D>& st, float (&s)[2][4], VAddr vaddr, int lane) {
   const float NEG = neg_inf();
@@ -104,16 +108,21 @@ __device__ __forceinline__ void softmax_pv16(RowState<D>& st, float (&s)[2][4], 
   }
   st.l[0] += pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1];
   st.l[1] += pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3];
-  const uint32_t pa[4] = {pack_bf16(pr[0][0], pr[0][1]), pack_bf16(pr[0][2], pr[0][3]),
-                          pack_bf16(pr[1][0], pr[1][1]), pack_bf16(pr[1][2], pr[1][3])};
+  uint32_t ph[4], pl[4];
+  split_bf16(pr[0][0], pr[0][1], ph[0], pl[0]);
+  split_bf16(pr[0][2], pr[0][3], ph[1], pl[1]);
+  split_bf16(pr[1][0], pr[1][1], ph[2], pl[2]);
+  split_bf16(pr[1][2], pr[1][3], ph[3], pl[3]);
   const int mi = lane >> 3, rr = lane & 7;
   const int r = (mi & 1) * 8 + rr;
 #pragma unroll
   for (int dn2 = 0; dn2 < D / 16; ++dn2) {
     uint32_t b0, b1, b2, b3;
     ldsm_x4_t(vaddr(r, dn2 * 2 + (mi >> 1)), b0, b1, b2, b3);
-    mma_bf16(st.o[2 * dn2], pa, b0, b1);
-    mma_bf16(st.o[2 * dn2 + 1], pa, b2, b3);
+    mma_bf16(st.o[2 * dn2], ph, b0, b1);
+    mma_bf16(st.o[2 * dn2 + 1], ph, b2, b3);
+    mma_bf16(st.o[2 * dn2], pl, b0, b1);
+    mma_bf16(st.o[2 * dn2 + 1], pl, b2, b3);
   }
 }
 

@@ -5,21 +5,32 @@
 // since; Vegas §3 (sparse execution) runs this as a paged attention with a page
 // of one token, the selected positions serving as page indices.
 //
-// GB300 design.  A token's page is its cache slot: all KV heads contiguous, H_kv*d*2
-// bytes of K and as many of V.  Each sequence's attended entries are its selected
-// positions followed by the tail of draft-token slots.  The work is the fixed grid
-// of (sequence, entry slot) items, k_stride + a tail bound slots per sequence (slots
-// past the sequence's entries are masked), split evenly over one persistent CTA per
-// SM: the split needs no device data, so each CTA's first memory round trip already
-// fetches its positions, and the combine kernel knows where the partials are.  A
-// producer warp turns each entry into two TMA bulk copies of a whole page (large
-// requests keep the copy engine efficient; the current draft token comes straight
-// from the inputs) landing in a padded, bank-conflict-free shared-memory ring
-// guarded by mbarriers; one consumer warp per KV head runs QK^T and PV on bf16
-// tensor cores with fp32 online softmax and writes one unnormalised partial per
-// (run, head).  A combine kernel (programmatic dependent launch) merges the
-// partials with 8 warps splitting them, writes bf16 outputs and appends the
-// current draft token's K/V to the cache.
+// GB300 design.
+//   * A token's page is its cache slot: all KV heads contiguous, H_kv*d*2 bytes of K
+//     and as many of V.  Each sequence's attended entries are its selected positions
+//     followed by the tail of draft-token slots.  The work is the fixed list of
+//     (sequence, entry slot) items - k_stride + a tail bound per sequence, slots past
+//     the sequence's entries masked - split evenly over one persistent CTA per SM, so
+//     the split needs no device data and each CTA's first round trip fetches its
+//     positions.
+//   * A producer warp turns each entry into two bulk copies of a whole page (large
+//     requests keep the copy engine efficient; the current draft token comes straight
+//     from the inputs) into a padded shared-memory ring guarded by mbarriers; one
+//     consumer warp per KV head runs Q K^T and P V on bf16 tensor cores with fp32
+//     online softmax, P carried as a bf16 high and low part.
+//   * Within a draft phase the selection does not change between steps.  When the
+//     caller says so (VG_DRAFT_SELECTION_SETTLED), the producer resolves its first
+//     chunks' positions and starts their page copies before the dependency wait, so
+//     the gather overlaps the end of the previous step; only the draft-token tail,
+//     which the previous step appended, waits for it.  Both kernels here release
+//     their dependents only after their own dependency wait, so no draft step starts
+//     before every kernel two launches back has completed.
+//   * A sequence whose entries one CTA holds entirely is finished by that CTA.  Every
+//     other (CTA, sequence) run leaves an unnormalised partial (O, max, sum), and a
+//     combine kernel (programmatic dependent launch) merges each (sequence, query
+//     head) in a fixed order.  No atomics: results are deterministic.
+//   * Whoever finishes a sequence's first query head of a KV head appends the current
+//     draft token's K/V row of that head to the cache.
 #include "attn_frag.cuh"
 #include "vg_common.cuh"
 #include "vg_internal.h"
@@ -27,9 +38,9 @@
 namespace vg {
 namespace {
 
-constexpr int kKeys = 16;  // entries per pipeline stage
+constexpr int kKeys = 16;  // entries per pipeline stage (one MMA key block)
 constexpr int kStages = 2;
-constexpr int kCombineRows = 12;  // partial rows a combine warp loads in its first round
+constexpr int kCombineRows = 12;  // partial rows a combine warp loads in one round
 
 struct DLayout {
   int row;  // bytes per gathered page in shared memory (padded by 16: ldmatrix rows hit distinct banks)
@@ -48,9 +59,79 @@ __device__ __forceinline__ int tail_len_of(const DraftParams& p, int b) {
   return p.tail_len ? p.tail_len[b] : p.tail_len_const;
 }
 
-// Entry slots per sequence in the static work split.
-__host__ __device__ __forceinline__ int draft_slots(const DraftParams& p) {
-  return p.k_stride + (p.tail_len ? kDraftMaxTail : p.tail_len_const);
+// Appends the current draft token's key and value of KV head g of sequence b at slot
+// tail_start + tail_len - 1 (threads t, t + nt, ... of a group; skipped, never
+// faulted, if out of range).
+template <int D>
+__device__ __forceinline__ void append_token(const DraftParams& p, int b, int g, int t, int nt) {
+  const int64_t off = p.seq_offset[b];
+  const int ts = p.tail_start[b];
+  const int tl = tail_len_of(p, b);
+  if (!(off >= 0 && ts >= 0 && tl >= 1 && tl <= kDraftMaxTail && off + ts + tl <= p.capacity)) return;
+  const size_t dst = ((off + ts + tl - 1) * p.Hkv + g) * D;
+  const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
+  for (int c = t; c < D / 8; c += nt) {
+    reinterpret_cast<uint4*>(p.K + dst)[c] = reinterpret_cast<const uint4*>(p.k_new + src)[c];
+    reinterpret_cast<uint4*>(p.V + dst)[c] = reinterpret_cast<const uint4*>(p.v_new + src)[c];
+  }
+}
+
+// The CTAs holding items of sequence b (first and last: the split is contiguous).
+struct SeqSpan {
+  int cf, cl;
+};
+__host__ __device__ __forceinline__ SeqSpan seq_span(int b, int S, int64_t E, int nctas) {
+  return SeqSpan{static_cast<int>(owner_cta(static_cast<int64_t>(b) * S, E, nctas)),
+                 static_cast<int>(owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, nctas))};
+}
+
+// One chunk entry as the producer warp resolves it (lane < nvalid: entry slot j + lane
+// of sequence b).  pos = -1 for a masked slot; tail marks a draft-token slot (appended
+// by earlier steps, or the current token, read from the inputs).
+struct ChunkPos {
+  int pos;
+  bool tail;
+  const __nv_bfloat16* ksrc;
+  const __nv_bfloat16* vsrc;
+};
+
+// (The loads bypass L1, cached at L2 only: with a settled selection they run before the
+// dependency wait, and must see what kernels that completed earlier wrote.)
+template <int D>
+__device__ __forceinline__ ChunkPos resolve(const DraftParams& p, int b, int j, int nvalid, int S, int lane) {
+  const int jj = j + lane;  // selected entries first, then the draft-token tail
+  const int cnt_raw = __ldcg(p.count + b);
+  const int tl = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
+  const int ts = __ldcg(p.tail_start + b);
+  const int64_t off = __ldcg(p.seq_offset + b);
+  const int sel = (lane < nvalid && jj < p.k_stride) ? __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj) : 0;
+  const bool seq_ok = cnt_raw >= 0 && cnt_raw <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && cnt_raw + tl <= S &&
+                      off >= 0 && ts >= 0 && off + ts + tl <= p.capacity && (p.k_new == nullptr || tl >= 1);
+  if (!seq_ok && lane == 0 && j == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
+  const int nsel = seq_ok ? cnt_raw : 0;
+  ChunkPos c{-1, false, nullptr, nullptr};
+  if (seq_ok && lane < nvalid) {
+    if (jj < nsel) {
+      c.pos = sel;
+      if (c.pos < 0 || c.pos >= ts) {
+        report(p.status, VG_ERR_DEVICE_BOUNDS);
+        c.pos = -1;
+      }
+    } else if (jj < nsel + tl) {
+      c.pos = ts + (jj - nsel);
+      c.tail = true;
+    }
+  }
+  if (c.pos >= 0) {
+    if (p.k_new && c.pos == ts + tl - 1) {  // the current draft token, straight from the inputs
+      c.ksrc = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
+      c.vsrc = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
+    } else {
+      c.ksrc = p.K + static_cast<size_t>(off + c.pos) * p.Hkv * D;
+      c.vsrc = p.V + static_cast<size_t>(off + c.pos) * p.Hkv * D;
+    }
+  }
+  return c;
 }
 
 // MAXW: the most KV heads (consumer warps) this instantiation serves.
@@ -79,74 +160,90 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   // the producer's critical path.
   for (int st = 0; st < kStages; ++st) {
     uint4* vr = reinterpret_cast<uint4*>(smem + st * L.stage + L.half);
-    for (int q = threadIdx.x; q < L.half / 16; q += blockDim.x) vr[q] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < L.half / 16; i += blockDim.x) vr[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async_smem();  // the zeros precede the bulk copies into the same stages
   __syncthreads();
-  const int S = draft_slots(p);
+  const int S = p.slots;
   const int64_t E = static_cast<int64_t>(p.B) * S;
   const int x0 = static_cast<int>(split_begin(blockIdx.x, E, p.nctas));
   const int x1 = static_cast<int>(split_begin(blockIdx.x + 1, E, p.nctas));
-  pdl_launch_dependents();
   if (x0 >= x1) return;
-  // idx / count come from the selection kernel, the tail pages from the previous step.
-  // Kernels of this library trigger their dependents early, so several may be in
-  // flight: nothing an earlier kernel writes is read before this wait.
-  pdl_wait();
   const int page = p.Hkv * D * 2;  // bytes of one token's K (or V), all heads
 
-  // ------------------------------------------------------------ producer warp
+  // ------------------------------------------------------------------ producer warp
   if (warp == W) {
     int b = x0 / S, j = x0 - b * S;
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;  // chunks whose copies were started
-    for (int x = x0; x < x1;) {
-      const int nvalid = min(kKeys, min(x1 - x, S - j));
-      bool ok_wait = true;
-      if (lane == 0) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
-      if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
-      // one round of independent loads: this sequence's counts and the chunk's positions
-      const int jj = j + lane;  // selected entries first, then the draft-token tail
-      const int cnt_raw = p.count[b];
-      const int tl = tail_len_of(p, b);
-      const int ts = p.tail_start[b];
-      const int64_t off = p.seq_offset[b];
-      const int sel = (lane < nvalid && jj < p.k_stride) ? p.idx[static_cast<size_t>(b) * p.k_stride + jj] : 0;
-      const bool seq_ok = cnt_raw >= 0 && cnt_raw <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && off >= 0 &&
-                          ts >= 0 && off + ts + tl <= p.capacity && (p.k_new == nullptr || tl >= 1);
-      if (!seq_ok && lane == 0 && j == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
-      const int nsel = seq_ok ? cnt_raw : 0;
-      uint8_t* kst = smem + stage * L.stage;
-      int pos = -1;
-      if (seq_ok && lane < nvalid) {
-        if (jj < nsel) {
-          pos = sel;
-          if (pos < 0 || pos >= ts) {
-            report(p.status, VG_ERR_DEVICE_BOUNDS);
-            pos = -1;
+    // With a settled selection the first kStages chunks' positions are resolved and
+    // their selected pages requested before the dependency wait; their tail pages (the
+    // previous step appended the last of them) and every later chunk wait for it.
+    ChunkPos early[kStages];
+    int nearly = 0;
+    if (p.settled) {
+      int bb = b, jj0 = j, x = x0;
+#pragma unroll
+      for (int i = 0; i < kStages; ++i) {
+        early[i] = ChunkPos{-1, false, nullptr, nullptr};
+        if (x < x1) {
+          const int nvalid = min(kKeys, min(x1 - x, S - jj0));
+          const ChunkPos c = resolve<D>(p, bb, jj0, nvalid, S, lane);
+          if (lane < kKeys) posb[i * kKeys + lane] = c.pos;
+          const int nload = __popc(__ballot_sync(0xffffffffu, c.pos >= 0));
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(nload * 2 * page));
+          __syncwarp();
+          if (c.pos >= 0 && !c.tail) {
+            uint8_t* kst = smem + i * L.stage;
+            bulk_load(kst + lane * L.row, c.ksrc, page, &full[i]);
+            bulk_load(kst + L.half + lane * L.row, c.vsrc, page, &full[i]);
           }
-        } else if (jj < nsel + tl) {
-          pos = ts + (jj - nsel);
+          early[i] = c;
+          nearly = i + 1;
+          x += nvalid;
+          jj0 += nvalid;
+          if (jj0 == S) {
+            jj0 = 0;
+            ++bb;
+          }
         }
       }
-      if (lane < kKeys) posb[stage * kKeys + lane] = pos;
-      const int nload = __popc(__ballot_sync(0xffffffffu, pos >= 0));
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nload * 2 * page));
-      __syncwarp();
-      if (pos >= 0) {
-        const __nv_bfloat16* ksrc;
-        const __nv_bfloat16* vsrc;
-        if (p.k_new && pos == ts + tl - 1) {  // the current draft token, straight from the inputs
-          ksrc = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
-          vsrc = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
-        } else {
-          ksrc = p.K + static_cast<size_t>(off + pos) * p.Hkv * D;
-          vsrc = p.V + static_cast<size_t>(off + pos) * p.Hkv * D;
+    }
+    // idx / count come from the selection kernel, the tail pages from the previous step:
+    // nothing an earlier kernel writes is read before this wait (but for the settled
+    // selection above, which the caller vouches for).  Dependents are released only
+    // after it, so when a later step starts its settled gather, every kernel before
+    // this one has completed (the selection kernel triggers at entry, and without this
+    // order a chain of early triggers could run a later step ahead of it).
+    pdl_wait();
+    pdl_launch_dependents();
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) {
+      if (i < nearly && early[i].pos >= 0 && early[i].tail) {
+        uint8_t* kst = smem + i * L.stage;
+        bulk_load(kst + lane * L.row, early[i].ksrc, page, &full[i]);
+        bulk_load(kst + L.half + lane * L.row, early[i].vsrc, page, &full[i]);
+      }
+    }
+    for (int x = x0; x < x1;) {
+      const int nvalid = min(kKeys, min(x1 - x, S - j));
+      if (issued >= nearly) {
+        bool ok_wait = true;
+        if (lane == 0 && issued >= kStages) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
+        if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
+        const ChunkPos c = resolve<D>(p, b, j, nvalid, S, lane);
+        if (lane < kKeys) posb[stage * kKeys + lane] = c.pos;
+        const int nload = __popc(__ballot_sync(0xffffffffu, c.pos >= 0));
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nload * 2 * page));
+        __syncwarp();
+        if (c.pos >= 0) {
+          uint8_t* kst = smem + stage * L.stage;
+          bulk_load(kst + lane * L.row, c.ksrc, page, &full[stage]);
+          bulk_load(kst + L.half + lane * L.row, c.vsrc, page, &full[stage]);
         }
-        bulk_load(kst + lane * L.row, ksrc, page, &full[stage]);
-        bulk_load(kst + L.half + lane * L.row, vsrc, page, &full[stage]);
       }
       ++issued;
       x += nvalid;
@@ -169,21 +266,24 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     return;
   }
 
-  // ------------------------------------------------------------ consumer warp: KV head g
+  // ------------------------------------------------------------------ consumer warp: KV head g
+  pdl_wait();  // (the queries are the call's inputs: read once the dependency resolved)
+  pdl_launch_dependents();
   const int g = warp;
   const int gid = lane >> 2, tig = lane & 3;
   int b = x0 / S, j = x0 - b * S;
   int stage = 0;
   uint32_t phase = 0;
   bool lost = false;
-  for (int x = x0; x < x1 && !lost;) {
+  for (int x = x0; x < x1;) {
+    const int run_x0 = x, run_j0 = j;
     const int seg_end = min(x1, x + (S - j));
     uint32_t qf[D / 16][4];
     load_q_frags<D>(qf, gid < p.G ? p.q + (static_cast<size_t>(b) * p.Hq + g * p.G + gid) * D : nullptr,
                     gid + 8 < p.G ? p.q + (static_cast<size_t>(b) * p.Hq + g * p.G + gid + 8) * D : nullptr, tig);
     RowState<D> st;
     st.init();
-    while (x < seg_end) {
+    while (x < seg_end && !lost) {
       const int nvalid = min(kKeys, seg_end - x);
       if (!mbar_wait(&full[stage], phase, p.status)) {
         lost = true;
@@ -216,27 +316,36 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
       x += nvalid;
       j += nvalid;
     }
-    // partial of this run for the G query heads of KV head g
+    if (lost) x = seg_end;  // (results of a lost wait are unspecified; the status says so)
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], 1);
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], 2);
     st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], 1);
     st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], 2);
-    const size_t id = static_cast<size_t>(blockIdx.x) + b;
+    const bool complete = run_j0 == 0 && seg_end - run_x0 == S;  // this CTA holds every entry of b
+    const size_t id = static_cast<size_t>(blockIdx.x) + b;       // (unique per (CTA, sequence) run)
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int jh = gid + half * 8;
       if (jh < p.G) {
-        const size_t r = id * p.Hq + g * p.G + jh;
+        const int h = g * p.G + jh;
+        if (complete) {
+          const float inv = st.l[half] > 0.f ? 1.f / st.l[half] : 0.f;
+          __nv_bfloat16* o = p.out + (static_cast<size_t>(b) * p.Hq + h) * D;
 #pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn)
-          *reinterpret_cast<float2*>(p.part_o + r * D + dn * 8 + tig * 2) =
-              make_float2(st.o[dn][half * 2], st.o[dn][half * 2 + 1]);
-        if (tig == 0) {
-          p.part_ml[r * 2 + 0] = st.m[half];
-          p.part_ml[r * 2 + 1] = st.l[half];
+          for (int dn = 0; dn < D / 8; ++dn)
+            *reinterpret_cast<__nv_bfloat162*>(o + dn * 8 + tig * 2) =
+                __floats2bfloat162_rn(st.o[dn][half * 2] * inv, st.o[dn][half * 2 + 1] * inv);
+        } else {
+          const size_t r = id * p.Hq + h;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; ++dn)
+            *reinterpret_cast<float2*>(p.part_o + r * D + dn * 8 + tig * 2) =
+                make_float2(st.o[dn][half * 2], st.o[dn][half * 2 + 1]);
+          if (tig == 0) *reinterpret_cast<float2*>(p.part_ml + r * 2) = make_float2(st.m[half], st.l[half]);
         }
       }
     }
+    if (complete && p.k_new) append_token<D>(p, b, g, lane, 32);
     if (x < x1) {
       j = 0;
       ++b;
@@ -244,49 +353,66 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   }
 }
 
-// One CTA per (query head h, sequence b), NW warps (enough that each holds at most
-// kCombineRows partials).  Warp w owns partials w, w + NW, ...: it loads their (max, sum) one per lane and their output rows (lanes across d)
-// in a single round, the CTA agrees on the global max through shared memory, and the
-// warps' weighted sums are added in a fixed order (deterministic).  The CTA of each
-// KV head's first query head then appends the current draft token.
+// Merge of the partials of (query head h, sequence b) = (blockIdx.x, blockIdx.y),
+// written by the CTAs cf..cl that hold some of b's entries (row c + b); nothing to do
+// when one CTA held all of them.  NW warps (4, 8 or 16, from the partial count): warp w
+// loads partials w, w + NW, ... in one round, the CTA agrees on their max and adds the
+// warps in a fixed order, then writes the bf16 output.  The CTA of each KV head's first
+// query head also appends the current draft token: the draft kernel writes none of
+// what that append reads (the token's row, the sequence's offsets), and every kernel
+// before the draft kernel completed before it released this one, so those loads are
+// issued before the dependency wait and leave the merge's critical path.
 template <int D, int NW>
 __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParams p) {
-  constexpr int kCombineWarps = NW;
-  constexpr int PER = D / 32;  // elements of a row per lane
-  __shared__ float red[kCombineWarps][D];
-  __shared__ float redl[kCombineWarps];
-  __shared__ float redm[kCombineWarps];
+  constexpr int PER = D / 32;
+  __shared__ float red[NW][D];
+  __shared__ float redl[NW], redm[NW];
   const int h = blockIdx.x, b = blockIdx.y;
-  const int g = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG = neg_inf();
-  // the partials of sequence b come from the CTAs whose static ranges meet its slots
-  const int S = draft_slots(p);
+  const int S = p.slots;
   const int64_t E = static_cast<int64_t>(p.B) * S;
-  const int64_t cf = owner_cta(static_cast<int64_t>(b) * S, E, p.nctas);
-  const int64_t cl = owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, p.nctas);
-  const int nseg = static_cast<int>(cl - cf + 1);  // <= 32 * kCombineWarps (host choice)
-  auto prow = [&](int si) { return (static_cast<size_t>(cf + si) + b) * p.Hq + h; };
-  pdl_launch_dependents();  // the next draft step may start its prologue
+  const SeqSpan sp = seq_span(b, S, E, p.nctas);
+  const int nseg = sp.cl - sp.cf + 1;
+  // the append (first query head of a KV head): the token's row and its slot, early
+  const bool app = p.k_new && h % p.G == 0 && nseg > 1 && tid < D / 8;
+  uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = kr;
+  int64_t adst = -1;
+  if (app) {
+    const int g = h / p.G;
+    const int64_t off = p.seq_offset[b];
+    const int ts = p.tail_start[b];
+    const int tl = tail_len_of(p, b);
+    const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
+    kr = reinterpret_cast<const uint4*>(p.k_new + src)[tid];
+    vr = reinterpret_cast<const uint4*>(p.v_new + src)[tid];
+    if (off >= 0 && ts >= 0 && tl >= 1 && tl <= kDraftMaxTail && off + ts + tl <= p.capacity)
+      adst = ((off + ts + tl - 1) * p.Hkv + g) * D;
+  }
+  // The next draft step may start once the draft kernel before this one completed: a
+  // step with a settled selection gathers before its own dependency wait, which is
+  // safe only when every kernel ahead of it in the chain has finished.
   pdl_wait();
+  pdl_launch_dependents();
+  if (nseg == 1) return;  // the one CTA holding b finished it
+  auto prow = [&](int si) { return (static_cast<size_t>(sp.cf + si) + b) * p.Hq + h; };
   // ---- one round of loads: lane q holds (max, sum) of partial warp + NW q; the first
   // kCombineRows output rows of the warp's partials go to registers
   float pm = NEG, pl = 0.f;
   {
-    const int si = warp + kCombineWarps * lane;
-    if (si < nseg && split_nonempty(cf + si, E, p.nctas)) {  // CTAs with no entries wrote no partial
+    const int si = warp + NW * lane;
+    if (si < nseg && split_nonempty(sp.cf + si, E, p.nctas)) {  // CTAs without entries wrote no partial
       const float2 v = *reinterpret_cast<const float2*>(p.part_ml + prow(si) * 2);
       pm = v.x;
       pl = v.y;
     }
   }
-  // (rows past nseg, or of a CTA with no entries, read as zeros: their weight is zero
-  // and the row holds whatever was there)
+  // (rows past nseg, or of a CTA without entries, read as zeros: their weight is zero)
   float v[kCombineRows][PER];
 #pragma unroll
   for (int q = 0; q < kCombineRows; ++q) {
-    const int si = warp + kCombineWarps * q;
-    const bool ok = si < nseg && split_nonempty(cf + si, E, p.nctas);
+    const int si = warp + NW * q;
+    const bool ok = si < nseg && split_nonempty(sp.cf + si, E, p.nctas);
     const float* src = p.part_o + prow(ok ? si : 0) * D + lane * PER;
     if constexpr (PER == 4) {
       const float4 x = ok ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -304,10 +430,10 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   __syncthreads();
   float M = NEG;
 #pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, redm[w]);
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, redm[w]);
   // ---- this warp's weighted sum, partials in order
   const float wt = (pm != NEG) ? ex2(pm - M) : 0.f;
-  float l = wt * pl;
+  float l = wt * pl;  // fixed-order butterfly
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   float acc[PER];
@@ -316,15 +442,15 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
 #pragma unroll
   for (int q = 0; q < kCombineRows; ++q) {
     const float wq = __shfl_sync(0xffffffffu, wt, q);
-    if (warp + kCombineWarps * q < nseg) {
+    if (warp + NW * q < nseg) {
 #pragma unroll
       for (int e = 0; e < PER; ++e) acc[e] += wq * v[q][e];
     }
   }
-  for (int q = kCombineRows; warp + kCombineWarps * q < nseg; ++q) {  // rare: more partials per warp
+  for (int q = kCombineRows; warp + NW * q < nseg; ++q) {  // rare: more partials a warp
     const float wq = __shfl_sync(0xffffffffu, wt, q);
-    if (!split_nonempty(cf + warp + kCombineWarps * q, E, p.nctas)) continue;  // (warp-uniform)
-    const float* src = p.part_o + prow(warp + kCombineWarps * q) * D + lane * PER;
+    if (!split_nonempty(sp.cf + warp + NW * q, E, p.nctas)) continue;  // (warp-uniform)
+    const float* src = p.part_o + prow(warp + NW * q) * D + lane * PER;
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] += wq * src[e];
   }
@@ -335,24 +461,15 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   if (tid < D) {
     float a = 0.f, lt = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {  // fixed order: deterministic
+    for (int w = 0; w < NW; ++w) {  // fixed order: deterministic
       a += red[w][tid];
       lt += redl[w];
     }
     p.out[(static_cast<size_t>(b) * p.Hq + h) * D + tid] = __float2bfloat16_rn(lt > 0.f ? a / lt : 0.f);
   }
-  if (p.k_new && h % p.G == 0) {  // append the current draft token at tail_start + tail_len - 1
-    const int64_t off = p.seq_offset[b];
-    const int ts = p.tail_start[b];
-    const int tl = tail_len_of(p, b);
-    if (off >= 0 && ts >= 0 && tl >= 1 && tl <= kDraftMaxTail && off + ts + tl <= p.capacity) {
-      const size_t dst = ((off + ts + tl - 1) * p.Hkv + g) * D;
-      const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
-      for (int c = tid; c < D / 8; c += kCombineWarps * 32) {
-        reinterpret_cast<uint4*>(p.K + dst)[c] = reinterpret_cast<const uint4*>(p.k_new + src)[c];
-        reinterpret_cast<uint4*>(p.V + dst)[c] = reinterpret_cast<const uint4*>(p.v_new + src)[c];
-      }
-    }
+  if (app && adst >= 0) {
+    reinterpret_cast<uint4*>(p.K + adst)[tid] = kr;
+    reinterpret_cast<uint4*>(p.V + adst)[tid] = vr;
   }
 }
 
@@ -371,37 +488,36 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW>, p);
-  if (e != cudaSuccess) return e;
-  // partials per sequence: the CTAs whose static ranges meet its slots
-  const int64_t E = static_cast<int64_t>(p.B) * draft_slots(p);
-  int nseg_max = 0;
-  for (int b = 0; b < p.B; ++b) {
-    const int64_t cf = owner_cta(static_cast<int64_t>(b) * draft_slots(p), E, p.nctas);
-    const int64_t cl = owner_cta(static_cast<int64_t>(b + 1) * draft_slots(p) - 1, E, p.nctas);
-    nseg_max = max(nseg_max, static_cast<int>(cl - cf + 1));
-  }
+  if ((e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW>, p)) != cudaSuccess) return e;
+  const int nw = draft_combine_warps(p.B, p.slots, p.nctas);
+  if (nw == 0) return cudaSuccess;  // every sequence was finished by the CTA holding it
   cudaLaunchConfig_t cfg2 = {};
   cfg2.gridDim = dim3(p.Hq, p.B);
-  cfg2.dynamicSmemBytes = 0;
+  cfg2.blockDim = dim3(nw * 32);
   cfg2.stream = stream;
   cfg2.attrs = at;
   cfg2.numAttrs = 1;
-  if (nseg_max <= 4 * kCombineRows) {
-    cfg2.blockDim = dim3(4 * 32);
-    return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 4>, p);
-  }
-  if (nseg_max <= 8 * kCombineRows) {
-    cfg2.blockDim = dim3(8 * 32);
-    return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 8>, p);
-  }
-  cfg2.blockDim = dim3(16 * 32);
+  if (nw == 4) return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 4>, p);
+  if (nw == 8) return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 8>, p);
   return cudaLaunchKernelEx(&cfg2, draft_combine_kernel<D, 16>, p);
 }
 
 }  // namespace
 
 size_t draft_smem_bytes(int D, int Hkv) { return static_cast<size_t>(DLayout(Hkv, D).total) + 128; }
+
+int draft_combine_warps(int B, int slots, int nctas) {
+  const int64_t E = static_cast<int64_t>(B) * slots;
+  int nseg_max = 0;
+  for (int b = 0; b < B; ++b) {
+    const SeqSpan sp = seq_span(b, slots, E, nctas);
+    nseg_max = max(nseg_max, sp.cl - sp.cf + 1);
+  }
+  if (nseg_max <= 1) return 0;
+  if (nseg_max <= 4 * kCombineRows) return 4;
+  if (nseg_max <= 8 * kCombineRows) return 8;
+  return 16;
+}
 
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl) {
   if (p.Hkv <= 8) {

@@ -155,15 +155,21 @@ vg_status check_mask(uint32_t mask, int R, const char* name) {
 // ---------------------------------------------------------------- workspace
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// CTAs of a draft step: one per SM (the combine gathers a sequence's partials in one
+// round with up to 16 warps of 12 rows each, and in later rounds beyond that).
+inline int draft_ctas(int sms) { return sms < 512 ? sms : 512; }
+
 struct WsLayout {
   size_t meta = 0, part_o = 0, part_ml = 0, part_s = 0;
-  size_t dmeta = 0, dpart_o = 0, dpart_ml = 0;
+  size_t dpart_o = 0, dpart_ml = 0, dend = 0;
   size_t total = 0;
 };
 
 // Row stride of the per-KV-head partial scores: 16-byte-aligned rows for vector stores.
 inline int score_stride(const Shape& s) { return (s.max_len + 63) & ~63; }
 
+// Workspace: the verify call's scratch; the draft step's partials reuse the same bytes
+// (the calls are stream-ordered).
 WsLayout ws_layout(const Shape& s, int sms) {
   WsLayout w;
   const size_t segs = static_cast<size_t>(sms) + static_cast<size_t>(s.B) * s.Hkv;
@@ -177,15 +183,14 @@ WsLayout ws_layout(const Shape& s, int sms) {
   w.part_s = off;
   off = up256(off + 2 * static_cast<size_t>(s.B) * s.Hkv * 2 * static_cast<size_t>(score_stride(s)) * 4);
   const size_t verify_total = off;
-  const size_t dsegs = static_cast<size_t>(sms) + s.B;
-  off = 0;  // the draft step's scratch reuses the same bytes (calls are stream-ordered)
-  w.dmeta = off;
-  off = up256(off + (static_cast<size_t>(s.B) + 1) * 4);
+  const size_t dsegs = static_cast<size_t>(draft_ctas(sms)) + s.B;  // (CTA, sequence) runs of a draft step
+  off = 0;
   w.dpart_o = off;
   off = up256(off + dsegs * s.Hq * s.D * 4);
   w.dpart_ml = off;
   off = up256(off + dsegs * s.Hq * 2 * 4);
-  w.total = verify_total > off ? verify_total : off;
+  w.dend = off;
+  w.total = verify_total > w.dend ? verify_total : w.dend;
   return w;
 }
 
@@ -323,6 +328,7 @@ struct DraftArgs {
   const int32_t *tail_start, *tail_len;
   int tail_len_const;
   void* out;
+  bool settled;
 };
 
 vg_status check_draft_args(const DraftArgs& a) {
@@ -332,7 +338,7 @@ vg_status check_draft_args(const DraftArgs& a) {
   if (!aligned16(a.q) || !aligned16(a.k_new) || !aligned16(a.v_new) || !aligned16(a.idx) || !aligned16(a.count) ||
       !aligned16(a.tail_start) || !aligned16(a.tail_len) || !aligned16(a.out))
     return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
-  if (a.k_stride < 1) return fail(VG_ERR_INVALID_ARG, "k_stride=%d < 1", a.k_stride);
+  if (a.k_stride < 1 || a.k_stride > (1 << 24)) return fail(VG_ERR_INVALID_ARG, "k_stride=%d outside [1, 2^24]", a.k_stride);
   return VG_OK;
 }
 
@@ -346,6 +352,7 @@ vg_status check_draft_page(const Shape& s) {
   return VG_OK;
 }
 
+// Pipeline stages of the draft kernel: two when they fit beside the run partials.
 vg_status check_draft_smem(const Shape& s, const DevInfo& di) {
   if (const vg_status st = check_draft_page(s); st != VG_OK) return st;
   if (draft_smem_bytes(s.D, s.Hkv) > di.smem_optin)
@@ -371,6 +378,7 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.tail_start = a.tail_start;
   p.tail_len = a.tail_len;
   p.tail_len_const = a.tail_len_const;
+  p.slots = a.k_stride + (a.tail_len ? kDraftMaxTail : a.tail_len_const);
   p.B = s.B;
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;
@@ -378,7 +386,8 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.D = s.D;
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
-  p.nctas = di.sms < 512 ? di.sms : 512;  // the combine gathers a sequence's partials in one round (<= 512)
+  p.settled = a.settled ? 1 : 0;
+  p.nctas = draft_ctas(di.sms);
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -458,7 +467,7 @@ vg_status iteration_prepare(const vg_dims* dims, const vg_kv_cache* cache, const
     return fail(VG_ERR_INVALID_ARG, "idx1 needs scores1 and 16-byte aligned idx1/count1");
   if (s.gamma > 0) {
     DraftArgs da{in->q_draft, in->k_draft, in->v_draft, out->idx, out->count, k, in->prefix_len, nullptr, 1,
-                 out->out_draft};
+                 out->out_draft, false};
     if (!in->k_draft || !in->v_draft) return fail(VG_ERR_INVALID_ARG, "k_draft and v_draft must be non-NULL");
     if ((st = check_draft_args(da)) != VG_OK) return st;
     if ((st = check_draft_page(s)) != VG_OK) return st;
@@ -500,7 +509,8 @@ vg_status iteration_enqueue(const IterCall& c, int32_t* dev_status, cudaStream_t
                  in->prefix_len,
                  nullptr,
                  step + 1,
-                 static_cast<char*>(out.out_draft) + step * qstep};
+                 static_cast<char*>(out.out_draft) + step * qstep,
+                 step > 0};  // (the selection was made before the previous step's kernels)
     if ((st = run_draft(s, c.cache, da, c.ws, c.w, c.di, dev_status, strm, true)) != VG_OK) return st;
   }
   return VG_OK;
@@ -534,6 +544,22 @@ vg_status vg_selftest_lost_wait(uint32_t limit_us, int32_t* dev_status, uint64_t
 }
 
 const char* vg_last_error(void) { return g_err.c_str(); }
+
+int32_t vg_sparse_draft_launches(const vg_dims* dims, int32_t k_stride, int32_t tail_len_max) {
+  g_err.clear();
+  Shape s;
+  if (check_dims(dims, &s) != VG_OK) return 0;
+  if (k_stride < 1 || k_stride > (1 << 24) || tail_len_max < 0 || tail_len_max > kDraftMaxTail) {
+    fail(VG_ERR_INVALID_ARG, "k_stride=%d or tail_len_max=%d out of range", k_stride, tail_len_max);
+    return 0;
+  }
+  if (check_draft_page(s) != VG_OK) return 0;
+  DevInfo di;
+  if (device_info(&di) != VG_OK) return 0;
+  if (check_draft_smem(s, di) != VG_OK) return 0;
+  const int slots = k_stride + (tail_len_max ? tail_len_max : kDraftMaxTail);
+  return draft_combine_warps(s.B, slots, draft_ctas(di.sms)) > 0 ? 2 : 1;
+}
 
 size_t vg_workspace_size(const vg_dims* dims, int32_t k) {
   Shape s;
@@ -581,15 +607,17 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
 
 vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q, const void* k_new,
                                const void* v_new, const int32_t* idx, const int32_t* count, int32_t k_stride,
-                               const int32_t* tail_start, const int32_t* tail_len, void* out, void* ws,
-                               size_t ws_bytes, int32_t* dev_status, void* stream) {
+                               const int32_t* tail_start, const int32_t* tail_len, uint32_t flags, void* out,
+                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
   g_err.clear();
   Shape s;
   vg_status st = check_dims(dims, &s);
   if (st != VG_OK) return st;
   if ((st = check_cache(cache)) != VG_OK) return st;
   if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
-  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
+  if (flags & ~VG_DRAFT_SELECTION_SETTLED) return fail(VG_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out,
+              (flags & VG_DRAFT_SELECTION_SETTLED) != 0};
   if ((st = check_draft_args(a)) != VG_OK) return st;
   if ((st = check_draft_page(s)) != VG_OK) return st;
   DevInfo di;
@@ -723,14 +751,13 @@ vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* c
   if (st != VG_OK) return st;
   if ((st = check_cache(cache)) != VG_OK) return st;
   if (!tail_len) return fail(VG_ERR_INVALID_ARG, "tail_len must be non-NULL");
-  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out};
+  DraftArgs a{q, k_new, v_new, idx, count, k_stride, tail_start, tail_len, 0, out, false};
   if ((st = check_draft_args(a)) != VG_OK) return st;
   if ((st = check_draft_page(s)) != VG_OK) return st;
   DevInfo di;
   if ((st = device_info(&di)) != VG_OK) return st;
   const WsLayout w = ws_layout(s, di.sms);
-  const size_t dsegs = static_cast<size_t>(di.sms) + s.B;
-  const size_t need = w.dpart_ml + dsegs * s.Hq * 2 * 4;  // end of the draft step's scratch
+  const size_t need = w.dend;  // end of the draft step's scratch
   if (need > kNoAllocScratchBytes)
     return fail(VG_ERR_WORKSPACE,
                 "no-allocation draft step needs %zu bytes of scratch for these dims; its built-in area holds %zu "

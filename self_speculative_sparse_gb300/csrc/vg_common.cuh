@@ -147,6 +147,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// Two fp32 -> their bf16 high parts (hi, packed) and the bf16 rounding of what the high
+// parts leave out (lo, packed): a + b = hi + lo to about 2^-17 relative.
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(a, b);
+  lo = pack_bf16(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
 // acc + lo + hi for a packed bf16 pair, each half widened exactly to fp32 (the
 // mixed-precision add of sm_100 and later: one instruction per element).
 __device__ __forceinline__ float add_bf16x2_f32(uint32_t w, float acc) {
@@ -244,6 +250,29 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 // ------------------------------------------------------------------ sync
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// ------------------------------------------------------------------ thread-block clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Split cluster barrier: every thread of every CTA of the cluster arrives once per
+// phase (release: its earlier writes, shared memory included, become visible to the
+// cluster) and waits before touching what the others wrote (acquire).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Generic address of the same shared-memory location in CTA `rank` of the cluster.
+template <typename T>
+__device__ __forceinline__ const T* map_rank(const T* p, uint32_t rank) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<const T*>(out);
 }
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue now / wait until the previous kernel's results are visible.

@@ -12,8 +12,11 @@ namespace vg {
 
 // Keys per verify tile: the unit of TMA transfer and of the work split.
 constexpr int kVerifyTileKeys = 64;
-// Longest draft-token tail a sparse draft step attends besides the selection.
-constexpr int kDraftMaxTail = 64;
+// Longest draft-token tail a sparse draft step attends besides the selection (the
+// draft tokens of one iteration number at most gamma + 1 <= 16).
+constexpr int kDraftMaxTail = 16;
+// Most CTAs in one thread-block cluster of the draft step.
+constexpr int kDraftMaxCluster = 16;
 // Largest sequence the top-k kernel holds (in shared memory, across a cluster of up to 16).
 constexpr int kTopkMaxLen = 262144;
 constexpr int kMaxBatch = 1024;
@@ -72,6 +75,8 @@ struct DraftParams {
   const int32_t* tail_start;   // [B]
   const int32_t* tail_len;     // [B] or null -> tail_len_const
   int tail_len_const;
+  int slots;                   // entry slots per sequence in the work split: k_stride + the tail bound
+  int settled;                 // the selection predates the previous kernel: gather before the wait
   int B, Hq, Hkv, G, D;
   float scale, scale_log2;
   int nctas;
@@ -89,5 +94,8 @@ cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, b
 size_t topk_smem_bytes(int per_cta);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
 size_t draft_smem_bytes(int D, int Hkv);
+// Warps of the draft step's combine kernel (4, 8 or 16 from the most partials a
+// sequence has), or 0 when every sequence's entries sit in one CTA (no combine runs).
+int draft_combine_warps(int B, int slots, int nctas);
 
 }  // namespace vg

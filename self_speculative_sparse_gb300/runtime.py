@@ -100,16 +100,24 @@ class LayerState:
         vb.vg_topk_select(sc, self.score_stride, self.prefix_len, self.B, self.max_len, self.k, idx, cnt,
                           dev_status=self.status, stream=stream)
 
-    def draft_step(self, s: int, tail_len: torch.Tensor, stream=None) -> None:
-        """Draft step s: attend idx U [n_b, n_b + s], appending draft token s at n_b + s."""
+    def draft_step(self, s: int, tail_len: torch.Tensor, stream=None, settled: bool | None = None) -> None:
+        """Draft step s: attend idx U [n_b, n_b + s], appending draft token s at n_b + s.
+
+        settled (default: s > 0): the selection was made before the kernel preceding this
+        call, as it is for every step of a draft phase after the first."""
+        settled = s > 0 if settled is None else settled
         vb.vg_sparse_draft_attn(self.dims, self.cache, self.q_draft[s], self.k_draft[s], self.v_draft[s], self.idx,
                                 self.count, self.k, self.prefix_len, tail_len, self.out_draft[s], self.ws,
-                                dev_status=self.status, stream=stream)
+                                dev_status=self.status, stream=stream,
+                                flags=vb.VG_DRAFT_SELECTION_SETTLED if settled else 0)
 
-    def launches_per_iteration(self, select_extra: bool = False) -> int:
-        """Kernels one vg_iteration enqueues: the verify kernel and its combine, one
-        selection (two with select_extra), and the draft kernels of each draft step."""
-        return 2 + (2 if select_extra and self.mask1 else 1) + self.gamma * vb.draft_launches(self.dims)
+    def launches_per_iteration(self, select_extra: bool = False, tail_from_device: bool = False) -> int:
+        """Kernels one iteration enqueues: the verify kernel and its combine, one selection
+        (two with select_extra), and each draft step's kernels (vg_iteration gives step s a
+        host-known tail of s + 1; the per-step calls here pass a device tail array)."""
+        draft = sum(vb.vg_sparse_draft_launches(self.dims, self.k, 0 if tail_from_device else s + 1)
+                    for s in range(self.gamma))
+        return 2 + (2 if select_extra and self.mask1 else 1) + draft
 
     def check_status(self) -> int:
         return int(self.status.item())

@@ -118,20 +118,21 @@ def test_topk_rejects_bad_arguments(lib):
 
 
 def test_draft_rejects_bad_arguments(lib):
-    def call(k_stride=16, tail_len=A, kn=A, vn=A, q=A, noalloc=False):
+    def call(k_stride=16, tail_len=A, kn=A, vn=A, q=A, noalloc=False, flags=0):
         d, c = dims(), cache()
         if noalloc:
             return lib.vg_sparse_draft_attn_noalloc(ctypes.byref(d), ctypes.byref(c), vb.ptr(q), vb.ptr(kn),
                                                     vb.ptr(vn), vb.ptr(A), vb.ptr(A), k_stride, vb.ptr(A),
                                                     vb.ptr(tail_len), vb.ptr(A), None, None)
         return lib.vg_sparse_draft_attn(ctypes.byref(d), ctypes.byref(c), vb.ptr(q), vb.ptr(kn), vb.ptr(vn),
-                                        vb.ptr(A), vb.ptr(A), k_stride, vb.ptr(A), vb.ptr(tail_len), vb.ptr(A),
-                                        vb.ptr(A), 1 << 30, None, None)
+                                        vb.ptr(A), vb.ptr(A), k_stride, vb.ptr(A), vb.ptr(tail_len), flags,
+                                        vb.ptr(A), vb.ptr(A), 1 << 30, None, None)
     for noalloc in (False, True):
         assert call(k_stride=0, noalloc=noalloc) == vb.VG_ERR_INVALID_ARG
         assert call(tail_len=None, noalloc=noalloc) == vb.VG_ERR_INVALID_ARG
         assert call(vn=None, noalloc=noalloc) == vb.VG_ERR_INVALID_ARG
         assert call(q=MIS, noalloc=noalloc) == vb.VG_ERR_INVALID_ARG
+    assert call(flags=2) == vb.VG_ERR_INVALID_ARG                      # unknown flag bit
 
 
 def test_iteration_rejects_bad_arguments(lib):
@@ -194,7 +195,7 @@ def test_draft_pages_above_1024_elements_are_refused_before_any_device_query(lib
     machine without a GPU the answer is VG_ERR_UNSUPPORTED_SHAPE, not VG_ERR_CUDA."""
     d, c = dims(B=1, H_q=H_kv, H_kv=H_kv, d=128, gamma=1, max_len=64), cache()
     code = lib.vg_sparse_draft_attn(ctypes.byref(d), ctypes.byref(c), vb.ptr(A), vb.ptr(A), vb.ptr(A), vb.ptr(A),
-                                    vb.ptr(A), 8, vb.ptr(A), vb.ptr(A), vb.ptr(A), vb.ptr(A), 1 << 30, None, None)
+                                    vb.ptr(A), 8, vb.ptr(A), vb.ptr(A), 0, vb.ptr(A), vb.ptr(A), 1 << 30, None, None)
     assert code == vb.VG_ERR_UNSUPPORTED_SHAPE
     code = lib.vg_sparse_draft_attn_noalloc(ctypes.byref(d), ctypes.byref(c), vb.ptr(A), vb.ptr(A), vb.ptr(A),
                                             vb.ptr(A), vb.ptr(A), 8, vb.ptr(A), vb.ptr(A), vb.ptr(A), None, None)
