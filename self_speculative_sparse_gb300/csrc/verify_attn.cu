@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsc = 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));  // score rows
-  const int arows = p.M + nsc;                                   // A-operand rows in use
+  const int arows = nsc ? p.sc_row0 + nsc : p.M;                 // A-operand rows in use
 
   // Launched as a programmatic dependent: shared and tensor memory are set up while
   // the previous kernel in the stream finishes; nothing in global memory (the
@@ -210,12 +210,15 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     fence_mbar_init();
   }
   if (warp == C::RWARPS + 1) tc_alloc(tmem_slot, C::TMEM_COLS);  // (and frees it at the end)
-  // A-operand rows no segment writes stay zero: Q rows >= arows, P rows >= M
+  // A-operand rows no segment writes stay zero: Q rows in [M, sc_row0) and >= arows,
+  // P rows >= M
   {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    const int qz = (MR - arows) * 8;
+    const int gap = nsc ? p.sc_row0 - p.M : 0;  // rows between the query rows and the score rows
+    const int qz = (MR - arows + gap) * 8;
     for (int e = threadIdx.x; e < C::HALVES * qz; e += C::THREADS) {
-      const int h = e / qz, r = arows + (e - h * qz) / 8, c = e & 7;
+      const int h = e / qz, k = (e - h * qz) / 8, c = e & 7;
+      const int r = k < gap ? p.M + k : arows + (k - gap);
       *reinterpret_cast<uint4*>(sQ + h * C::QHALF + r * 128 + c * 16) = z;
     }
     const int pz = (MR - p.M) * 8;
@@ -342,7 +345,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     const uint32_t tl = tm + (static_cast<uint32_t>(32 * quad) << 16);
     const bool wact = QR * quad < arows;  // warp-uniform: lanes hold rows in use
     const bool is_row = row < p.M;
-    const int sci = row - p.M;
+    const int sci = row - p.sc_row0;
     const bool is_sc = sci >= 0 && sci < nsc;
     const int sc_ms = (sci >> 1) == 0 && p.mask0 ? 0 : 1;  // score rows: mask0 first if in use
     const int sc_part = sci & 1;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
           const __nv_bfloat16 lo = __float2bfloat16_rn(acc - bf2f(hi));
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
-            const int r = p.M + 2 * a + part;
+            const int r = p.sc_row0 + 2 * a + part;
             *reinterpret_cast<__nv_bfloat16*>(sQ + (rtid >> 6) * C::QHALF + r * 128 + (((cc >> 3) ^ (r & 7)) << 4) +
                                               (cc & 7) * 2) = part ? lo : hi;
           }
@@ -1080,6 +1083,14 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
 
 }  // namespace
 
+int verify_sc_row0(int M, int nsc) {
+  if (nsc == 0) return M;
+  const int MR = M + nsc <= 64 ? 64 : 128;  // the MMA shape the packed rows need
+  const int QR = MR / 4;                    // rows a lane quadrant holds
+  const int r0 = (M + QR - 1) / QR * QR;
+  return r0 + nsc <= MR ? r0 : M;
+}
+
 size_t verify_smem_bytes(int D, int B) {
   auto mx = [](size_t a, size_t b) { return a > b ? a : b; };
   if (D == 64) return mx(TCfg<64, 64>::smem(B), TCfg<64, 128>::smem(B));
@@ -1090,7 +1101,8 @@ size_t verify_smem_bytes(int D, int B) {
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream) {
   // A-operand rows: the query rows, then a high and a low row per score mask
-  const int arows = p.M + 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));
+  const int nsc = 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));
+  const int arows = nsc ? p.sc_row0 + nsc : p.M;
   if (arows <= 64) {
     if (p.D == 64) return launch_verify_t<64, 64>(p, tmK, tmV, stream);
     if (p.D == 128) return launch_verify_t<128, 64>(p, tmK, tmV, stream);

@@ -260,6 +260,7 @@ vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, 
   p.D = s.D;
   p.M = s.M;
   p.Mpad = s.Mpad;
+  p.sc_row0 = verify_sc_row0(s.M, 2 * ((a.mask0 ? 1 : 0) + (a.mask1 ? 1 : 0)));
   p.max_len = s.max_len;
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;

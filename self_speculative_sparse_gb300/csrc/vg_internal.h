@@ -31,6 +31,7 @@ struct VerifyParams {
   const int32_t* prefix_len;   // [B]
   int64_t capacity;
   int B, Hq, Hkv, G, R, D, M, Mpad;  // M = G * R rows per KV head, Mpad = 16 * ceil(M / 16)
+  int sc_row0;       // first score row of the MMA's A operand (after the query rows, see verify_sc_row0)
   int max_len;
   float scale;       // natural-log units (scores)
   float scale_log2;  // scale * log2(e) (softmax)
@@ -89,6 +90,11 @@ struct DraftParams {
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream);
+// First score row of the verify MMA's A operand for M query rows and nsc score rows: the
+// start of the next lane quadrant (16 rows at M = 64, 32 at M = 128) when the rows still
+// fit the same MMA shape, so that the score rows' stores fall to row warps that hold no
+// query row; else right after the query rows.
+int verify_sc_row0(int M, int nsc);
 size_t verify_smem_bytes(int D, int B);
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
 size_t topk_smem_bytes(int per_cta);
