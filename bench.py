@@ -501,6 +501,18 @@ def selection_stats(S: Setup, score_us: dict, ph: dict, iter_us: float) -> dict:
     out = {"score_emission_us": emit, "select_us": ph["select"],
            "selection_overhead_pct": 100.0 * (emit + ph["select"]) / iter_us,
            "note": "(verify with the selection mask - verify without scores + top-k) / iteration"}
+    # the query-agnostic comparison policy (a sliding window of the last k positions)
+    # against the verification-guided selection of the same layer
+    from self_speculative_sparse_gb300 import binding as vb
+    st = S.states[0]
+    idx_w = torch.empty_like(st.idx)
+    cnt_w = torch.empty_like(st.count)
+    vb.vg_window_select(st.prefix_len, w.B, st.max_len, st.k, idx_w, cnt_w, dev_status=st.status)
+    torch.cuda.synchronize()
+    iv, cv, iw = st.idx.cpu().numpy(), st.count.cpu().numpy(), idx_w.cpu().numpy()
+    ovw = [overlap_fraction(iv[b, :int(cv[b])], iw[b, :int(cv[b])], int(cv[b])) for b in range(w.B)]
+    out["overlap_window_vs_" + w.select_rows] = {"mean": float(sum(ovw) / len(ovw)), "min": float(min(ovw)),
+                                                 "sequences": len(ovw)}
     if w.extra_rows:
         ov = []
         for st in S.states[:1]:

@@ -140,6 +140,22 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
                          size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Sliding-window selection: the query-agnostic comparison policy of Vegas §1 (simple
+ * query-agnostic methods such as sliding windows select cheaply but draft poorly).
+ * No counterpart in the Vegas method itself; it gives drafts a baseline selection in
+ * the same form as vg_topk_select, whose overlap with the verification-guided one can
+ * be measured.
+ *
+ *   T_b = the last min(k, len[b]) prefix positions, len[b] - count_b .. len[b] - 1,
+ *   idx[b][0..count_b) = T_b ascending, idx[b][count_b..k) = -1, count[b] = count_b.
+ *
+ *   len  device int32 [B], each in [0, max_len] (others: VG_ERR_DEVICE_BOUNDS, count 0)
+ *   idx  int32 [B][k];  count  int32 [B];  1 <= k <= 2^24
+ */
+vg_status vg_window_select(const int32_t* len, int32_t B, int32_t max_len, int32_t k, int32_t* idx,
+                           int32_t* count, int32_t* dev_status, void* stream);
+
+/*
  * One sparse draft step (Vegas §2 step 3; §3 sparse execution with page size one).
  *
  * For sequence b the attended set is

@@ -16,6 +16,7 @@ from .vegas import (  # noqa: F401
     aggregated_scores,
     aggregated_scores_grouped,
     select_topk,
+    select_window,
     sparse_draft_attention,
     draft_step,
     iteration,

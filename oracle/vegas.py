@@ -166,6 +166,15 @@ def select_topk(s: np.ndarray, k: int) -> np.ndarray:
     return np.sort(order[:m]).astype(np.int64)
 
 
+def select_window(n: int, k: int) -> np.ndarray:
+    """The query-agnostic baseline of Vegas §1 (problem statement: sliding windows select
+    cheaply but draft poorly): the last min(k, n) prefix positions, ascending (int64)."""
+    if k < 0 or n < 0:
+        raise ValueError("n and k must be >= 0")
+    m = min(k, n)
+    return np.arange(n - m, n, dtype=np.int64)
+
+
 def selection_overlap(a: np.ndarray, b: np.ndarray, k: int) -> float:
     """|A ∩ B| / k: how much two selections agree (Vegas §2.B observation)."""
     if k <= 0:

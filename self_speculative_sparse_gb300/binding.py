@@ -22,7 +22,7 @@ VG_ERR_CUDA = -4
 VG_ERR_DEVICE_TIMEOUT = -5
 VG_ERR_DEVICE_BOUNDS = -6
 
-ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_sparse_draft_attn", "vg_iteration",
+ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_window_select", "vg_sparse_draft_attn", "vg_iteration",
                 "vg_iteration_plan_create", "vg_iteration_plan_launch", "vg_iteration_plan_destroy",
                 "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_sparse_draft_launches",
                 "vg_last_error", "vg_version", "vg_selftest_lost_wait")
@@ -75,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_verify_attn.restype = i32
     L.vg_topk_select.argtypes = [vp, i64, vp, i32, i32, i32, vp, vp, vp, sz, vp, vp]
     L.vg_topk_select.restype = i32
+    L.vg_window_select.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
+    L.vg_window_select.restype = i32
     L.vg_sparse_draft_attn.argtypes = [ctypes.POINTER(vg_dims), ctypes.POINTER(vg_kv_cache), vp, vp, vp, vp, vp,
                                        i32, vp, vp, u32, vp, vp, sz, vp, vp]
     L.vg_sparse_draft_attn.restype = i32
@@ -166,6 +168,11 @@ def vg_topk_select(scores, score_stride, len_, B, max_len, k, idx, count, ws=Non
                    dev_status=None, stream=None) -> None:
     _check(load().vg_topk_select(ptr(scores), score_stride, ptr(len_), B, max_len, k, ptr(idx), ptr(count),
                                  ptr(ws), ws_bytes, ptr(dev_status), _stream(stream)))
+
+
+def vg_window_select(len_, B, max_len, k, idx, count, dev_status=None, stream=None) -> None:
+    """The last min(k, len) positions of each sequence (the sliding-window baseline)."""
+    _check(load().vg_window_select(ptr(len_), B, max_len, k, ptr(idx), ptr(count), ptr(dev_status), _stream(stream)))
 
 
 VG_DRAFT_SELECTION_SETTLED = 1

@@ -324,7 +324,41 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   }
 }
 
+// The query-agnostic comparison policy (Vegas §1, problem statement: simple
+// query-agnostic selections such as sliding windows cost little to select but draft
+// poorly): the last k prefix positions of each sequence, in the same output form as
+// the score-based selection.  Grid (ceil(k / 256), B).
+__global__ void __launch_bounds__(256) window_kernel(const int32_t* len, int B, int max_len, int k, int32_t* idx,
+                                                     int32_t* count, int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.y;
+  int n = len[b];
+  if (n < 0 || n > max_len) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report(status, VG_ERR_DEVICE_BOUNDS);
+    n = 0;
+  }
+  const int cnt = min(k, n);
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < k) idx[static_cast<size_t>(b) * k + i] = i < cnt ? n - cnt + i : -1;
+  if (i == 0) count[b] = cnt;
+}
+
 }  // namespace
+
+cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t* idx, int32_t* count,
+                          int32_t* status, cudaStream_t stream) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((k + 255) / 256, B);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, window_kernel, len, B, max_len, k, idx, count, status);
+}
 
 size_t topk_smem_bytes(int per_cta) {
   return static_cast<size_t>(per_cta) * 4 + static_cast<size_t>(kWarps + 2 * kMaxCluster) * kBins * 4 +

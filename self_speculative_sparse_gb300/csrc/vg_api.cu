@@ -606,6 +606,21 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
                   static_cast<cudaStream_t>(stream), true);
 }
 
+vg_status vg_window_select(const int32_t* len, int32_t B, int32_t max_len, int32_t k, int32_t* idx, int32_t* count,
+                           int32_t* dev_status, void* stream) {
+  g_err.clear();
+  if (!len || !idx || !count) return fail(VG_ERR_INVALID_ARG, "len, idx and count must be non-NULL");
+  if (!aligned16(len) || !aligned16(idx) || !aligned16(count))
+    return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0) return fail(VG_ERR_INVALID_ARG, "dev_status must be 4-byte aligned");
+  if (B < 1 || B > kMaxBatch) return fail(VG_ERR_UNSUPPORTED_SHAPE, "B=%d outside [1, %d]", B, kMaxBatch);
+  if (max_len < 0) return fail(VG_ERR_INVALID_ARG, "max_len=%d < 0", max_len);
+  if (k < 1 || k > (1 << 24)) return fail(VG_ERR_INVALID_ARG, "k=%d outside [1, 2^24]", k);
+  const cudaError_t e = launch_window(len, B, max_len, k, idx, count, dev_status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "window selection launch");
+  return VG_OK;
+}
+
 vg_status vg_sparse_draft_attn(const vg_dims* dims, const vg_kv_cache* cache, const void* q, const void* k_new,
                                const void* v_new, const int32_t* idx, const int32_t* count, int32_t k_stride,
                                const int32_t* tail_start, const int32_t* tail_len, uint32_t flags, void* out,

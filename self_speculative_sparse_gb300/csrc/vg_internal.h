@@ -98,6 +98,8 @@ int verify_sc_row0(int M, int nsc);
 size_t verify_smem_bytes(int D, int B);
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl);
 size_t topk_smem_bytes(int per_cta);
+cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t* idx, int32_t* count,
+                          int32_t* status, cudaStream_t stream);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
 size_t draft_smem_bytes(int D, int Hkv);
 // Warps of the draft step's combine kernel (4, 8 or 16 from the most partials a

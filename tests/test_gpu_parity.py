@@ -337,3 +337,25 @@ def test_a_lost_wait_reports_a_timeout_and_the_gpu_stays_usable():
     torch.cuda.synchronize()
     assert st.check_status() == 0
     check_iteration(w, pool, st, w.rows(w.select_rows), w.rows(w.extra_rows) if w.extra_rows else None)
+
+
+def test_window_selection_matches_oracle():
+    """The sliding-window comparison policy (Vegas §1): bit-exact against the oracle,
+    with prefixes shorter than, equal to and longer than k, empty, and several CTAs of k."""
+    from self_speculative_sparse_gb300 import binding as vb
+    lens = [0, 1, 5, 300, 301, 999, 70000]
+    B, L = len(lens), max(lens)
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k in (1, 300, 700):
+        idx = torch.full((B, k), 7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+        vb.vg_window_select(lt, B, L, k, idx, cnt, dev_status=status)
+        torch.cuda.synchronize()
+        gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+        for b, n in enumerate(lens):
+            want = oracle.select_window(n, k)
+            assert gc[b] == len(want), (k, b)
+            assert np.array_equal(gi[b, :len(want)], want), (k, b)
+            assert (gi[b, len(want):] == -1).all(), (k, b)
+    assert int(status.item()) == 0

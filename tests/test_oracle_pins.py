@@ -323,6 +323,26 @@ def test_overlap_of_selections_with_k_at_least_n_is_one():
     assert oracle.selection_overlap(ta, tb, min(20, 9)) == 1.0
 
 
+# ------------------------------------------------------------ sliding window
+# Vegas §1 (problem statement): the query-agnostic comparison policy, a sliding window
+# of the most recent entries.
+def test_window_hand_cases():
+    assert oracle.select_window(10, 3).tolist() == [7, 8, 9]
+    assert oracle.select_window(2, 5).tolist() == [0, 1]
+    assert oracle.select_window(0, 4).tolist() == []
+    assert oracle.select_window(6, 6).tolist() == [0, 1, 2, 3, 4, 5]
+
+
+def test_window_is_the_topk_of_a_recency_score():
+    # with scores that grow with the position, the score-based selection (the argmax of
+    # Vegas §2.A, checked by exhaustive search above) picks exactly the window
+    r = np.random.default_rng(23)
+    for _ in range(50):
+        n, k = int(r.integers(1, 60)), int(r.integers(1, 70))
+        s = np.cumsum(r.uniform(0.01, 1.0, size=n))
+        assert oracle.select_topk(s, k).tolist() == oracle.select_window(n, k).tolist()
+
+
 # ------------------------------------------------------------ planted mistakes
 def _pin_errors(mod):
     """Discrepancies of the pins above for a (possibly mutated) oracle module."""
@@ -349,12 +369,14 @@ def _pin_errors(mod):
     sparse = mod.draft_step(q[2], K, V, np.arange(n), kn[:3], vn[:3])
     errs["k_eq_n"] = np.abs(dense - sparse).max()
     errs["overlap"] = abs(mod.selection_overlap(np.array([0, 2, 4, 6]), np.array([2, 3, 4, 5]), 4) - 0.5)
+    errs["window"] = int(mod.select_window(10, 3).tolist() != [7, 8, 9]) + int(
+        mod.select_topk(np.arange(1.0, 13.0), 5).tolist() != mod.select_window(12, 5).tolist())
     return errs
 
 
 def _caught(errs):
     return (errs["sdpa"] > 1e-9 or errs["linearity"] > 1e-9 or errs["worked"] > 1e-9
-            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9 or errs["overlap"] > 0)
+            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9 or errs["overlap"] > 0 or errs["window"] > 0)
 
 
 def test_unmutated_oracle_passes_every_pin():
@@ -371,6 +393,8 @@ MUTANTS = {
     "draft drops the current token": ("draft_step", None, None),
     "overlap over the union (Jaccard)": ("selection_overlap", None, None),
     "overlap over the larger total": ("selection_overlap", None, None),
+    "window one position early": ("select_window", None, None),
+    "window at the start": ("select_window", None, None),
 }
 
 
@@ -430,6 +454,15 @@ def _mutant(name):
         def selection_overlap(a, b, k):
             return len(np.intersect1d(a, b)) / float(len(a) + len(b)) if k > 0 else 1.0
         m.selection_overlap = selection_overlap
+    elif name == "window one position early":
+        def select_window(n, k):
+            m_ = min(k, n)
+            return np.arange(max(0, n - m_ - 1), max(0, n - 1), dtype=np.int64)
+        m.select_window = select_window
+    elif name == "window at the start":
+        def select_window(n, k):
+            return np.arange(0, min(k, n), dtype=np.int64)
+        m.select_window = select_window
     return m
 
 
