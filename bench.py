@@ -547,6 +547,44 @@ def secondary_line(name: str, local: int, steps: int, peak: float) -> dict:
     return out
 
 
+ACCEPT_VOCAB = 151936  # a Qwen3-family vocabulary (the pages' models)
+
+
+def accept_timing(w, local: int, steps: int, peak: float) -> dict:
+    """The acceptance step after verification (greedy and speculative sampling) on
+    synthetic logits of the workload's batch and gamma, vocabulary ACCEPT_VOCAB."""
+    import torch
+    import synth
+    from self_speculative_sparse_gb300 import binding as vb
+    B, gamma, V = w.B, w.gamma, ACCEPT_VOCAB
+    inp = synth.accept_inputs(B, gamma, V, seed=7)
+    dev = f"cuda:{local}"
+    t = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    na = torch.empty(B, dtype=torch.int32, device=dev)
+    nt = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(vb.vg_accept_workspace_size(B, gamma, V), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    out = {"workload": f"B={B} gamma={gamma} V={V}, fp32 logits"}
+    for mode, nm in ((vb.VG_ACCEPT_GREEDY, "greedy"), (vb.VG_ACCEPT_SAMPLE, "sample")):
+        def call():
+            vb.vg_accept(B, gamma, V, t["p_logits"], t["q_logits"], t["x"], t["u"], t["u_res"], mode, na, nt, None,
+                         ws, dev_status=status)
+        call()
+        torch.cuda.synchronize()
+        g = capture(lambda: [call() for _ in range(steps)])
+        us = time_graph_us(g, stream, steps)
+        del g
+        rows = B * (gamma + 1) + (B * gamma if mode == vb.VG_ACCEPT_SAMPLE else 0)
+        nbytes = rows * V * 4 + (B * 2 * V * 4 if mode == vb.VG_ACCEPT_SAMPLE else 0)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[nm] = {"us": us, "bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peak,
+                   "mean_accepted": float(na.float().mean().item())}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the acceptance step")
+    return out
+
+
 def run_ours(args, rank, local, world):
     import torch
     import synth
@@ -746,6 +784,8 @@ def run_ours(args, rank, local, world):
     del staged, plans, S
     torch.cuda.empty_cache()
 
+    if rank == 0:
+        line["accept_step_us"] = accept_timing(w, local, args.steps, peaks["hbm_gbs"])
     names = args.secondary if args.secondary is not None else (SECONDARY if args.workload == DEFAULT_WORKLOAD
                                                                else "none")
     if rank == 0 and names != "none":

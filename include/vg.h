@@ -284,6 +284,38 @@ vg_status vg_sparse_draft_attn_noalloc(const vg_dims* dims, const vg_kv_cache* c
                                        const int32_t* count, int32_t k_stride, const int32_t* tail_start,
                                        const int32_t* tail_len, void* out, int32_t* dev_status, void* stream);
 
+/*
+ * Acceptance of the draft chain (Vegas §2 step 1: the verification pass accepts or
+ * rejects the draft tokens; §5: lossless, what is committed follows the target model).
+ * The page leaves the rule to standard speculative decoding; this is that rule on
+ * given logits.  For sequence b:
+ *   p_logits  fp32 [B][gamma+1][V]  row t: the target's logits for the token after t
+ *                                     accepted drafts (row gamma: the bonus position)
+ *   q_logits  fp32 [B][gamma][V]    the draft's logits of draft token t (sampling only)
+ *   draft_tokens  int32 [B][gamma]  in [0, V) (others: rejected, VG_ERR_DEVICE_BOUNDS)
+ *   mode VG_ACCEPT_GREEDY: draft t survives while it is the most likely token of row t
+ *     (ties: lowest token); the next token is the most likely token of row a.
+ *   mode VG_ACCEPT_SAMPLE: draft t survives iff u_accept[b][t] * q_t(x_t) < p_t(x_t), p and
+ *     q the softmax of the rows; at the first rejection a the next token is drawn from
+ *     max(0, p_a - q_a) (from p_a if that is zero everywhere), after gamma acceptances
+ *     from p_gamma.  A draw with weights w takes the smallest v whose running sum of
+ *     weights exceeds u_resample[b] times their total.  u values in [0, 1), fp32.
+ *   n_accept  int32 [B]: a, the drafts accepted (0 .. gamma);  next_token int32 [B].
+ *   advance_len  int32 [B] or NULL: if given, increased by a + 1 (the verified row before
+ *     the drafts and the a accepted drafts join the prefix; their keys and values are
+ *     already in the cache).
+ * Computed in fp32 with fixed summation orders (deterministic).  B <= 1024, gamma <= 15,
+ * V <= 2^20; V % 4 == 0 reads the rows with 16-byte loads.  Workspace: at least
+ * vg_accept_workspace_size(B, gamma, V) bytes, 256-byte aligned, no initialisation.
+ */
+#define VG_ACCEPT_GREEDY 0u
+#define VG_ACCEPT_SAMPLE 1u
+size_t vg_accept_workspace_size(int32_t B, int32_t gamma, int32_t V);
+vg_status vg_accept(int32_t B, int32_t gamma, int32_t V, const float* p_logits, const float* q_logits,
+                    const int32_t* draft_tokens, const float* u_accept, const float* u_resample,
+                    uint32_t mode, int32_t* n_accept, int32_t* next_token, int32_t* advance_len,
+                    void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Bytes of workspace any call above needs for these dimensions on the current
  * device (0 on invalid dims or no device; see vg_last_error()). */
 size_t vg_workspace_size(const vg_dims* dims, int32_t k);

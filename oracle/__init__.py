@@ -16,9 +16,15 @@ from .vegas import (  # noqa: F401
     aggregated_scores,
     aggregated_scores_grouped,
     select_topk,
-    select_window,
     sparse_draft_attention,
     draft_step,
     iteration,
     selection_overlap,
+    select_window,
+    softmax,
+    sample_inverse_cdf,
+    argmax_lowest,
+    accept_greedy,
+    accept_sample,
+    next_prefix_len,
 )

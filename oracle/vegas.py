@@ -229,3 +229,66 @@ def iteration(q_verify, K, V, k_new, v_new, q_draft, k_draft, v_draft, k: int,
     for s in range(gamma):
         O_d[s] = draft_step(q_draft[s], K, V, T, k_draft[:s + 1], v_draft[:s + 1], scale)
     return dict(out_verify=O_v, scores0=s0, scores1=s1, idx=T, out_draft=O_d)
+
+
+# ------------------------------------------------------------------ acceptance
+# Vegas §2 step 1 (verification phase: the target's full-attention pass decides which
+# draft tokens are accepted) and §5 (lossless quality: the output follows the target
+# model's distribution).  The page names acceptance without spelling out the rule; the
+# rule written here is the standard one of speculative decoding (greedy: a draft token
+# survives if it is the target's most likely token; sampling: accept x with probability
+# min(1, p(x) / q(x)), resample a rejection from the normalised excess max(0, p - q)).
+# Layout: p_logits [gamma+1][V] (row t: the target's distribution for the token after t
+# accepted drafts; row gamma: the bonus position), q_logits [gamma][V] (the draft's
+# distribution of draft token t), draft tokens x [gamma].
+
+def softmax(logits: np.ndarray) -> np.ndarray:
+    """exp(l - max l) / sum exp(l - max l) along the last axis (float64)."""
+    l = np.asarray(logits, dtype=np.float64)
+    e = np.exp(l - l.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def sample_inverse_cdf(w: np.ndarray, u: float) -> int:
+    """The smallest v with sum_{i <= v} w_i > u * sum_i w_i (weights >= 0, not all zero;
+    a token of weight zero is never drawn).  u in [0, 1)."""
+    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    return int(np.searchsorted(c, u * c[-1], side="right"))
+
+
+def argmax_lowest(v: np.ndarray) -> int:
+    """Position of the largest value; ties go to the lowest position."""
+    v = np.asarray(v)
+    return int(np.flatnonzero(v == v.max())[0])
+
+
+def accept_greedy(p_logits: np.ndarray, x: np.ndarray) -> tuple[int, int]:
+    """(accepted count a, next token): draft t is kept while x_t is the target's most
+    likely token at row t; the next token is that most likely token at row a."""
+    gamma = len(x)
+    a = 0
+    while a < gamma and int(x[a]) == argmax_lowest(p_logits[a]):
+        a += 1
+    return a, argmax_lowest(p_logits[a])
+
+
+def accept_sample(p_logits: np.ndarray, q_logits: np.ndarray, x: np.ndarray, u: np.ndarray,
+                  u_res: float) -> tuple[int, int]:
+    """(accepted count a, next token) by speculative sampling.  Draft t is accepted iff
+    u_t * q_t(x_t) < p_t(x_t).  At the first rejection a the next token is drawn from the
+    excess max(0, p_a - q_a) (from p_a if that is zero everywhere); after gamma
+    acceptances it is drawn from p_gamma; both by inverse CDF with u_res."""
+    gamma = len(x)
+    for t in range(gamma):
+        p, q = softmax(p_logits[t]), softmax(q_logits[t])
+        xt = int(x[t])
+        if not (u[t] * q[xt] < p[xt]):
+            w = np.maximum(0.0, p - q)
+            return t, sample_inverse_cdf(w if w.sum() > 0 else p, u_res)
+    return gamma, sample_inverse_cdf(softmax(p_logits[gamma]), u_res)
+
+
+def next_prefix_len(n: int, a: int) -> int:
+    """Prefix length after acceptance: the verified row before the drafts and the a
+    accepted drafts enter the prefix (their keys and values are already in the cache)."""
+    return n + a + 1

@@ -25,6 +25,7 @@ VG_ERR_DEVICE_BOUNDS = -6
 ENTRY_POINTS = ("vg_verify_attn", "vg_topk_select", "vg_window_select", "vg_sparse_draft_attn", "vg_iteration",
                 "vg_iteration_plan_create", "vg_iteration_plan_launch", "vg_iteration_plan_destroy",
                 "vg_sparse_draft_attn_noalloc", "vg_workspace_size", "vg_sparse_draft_launches",
+                "vg_accept", "vg_accept_workspace_size",
                 "vg_last_error", "vg_version", "vg_selftest_lost_wait")
 
 
@@ -96,6 +97,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.vg_iteration_plan_destroy.restype = i32
     L.vg_workspace_size.argtypes = [ctypes.POINTER(vg_dims), i32]
     L.vg_workspace_size.restype = sz
+    L.vg_accept_workspace_size.argtypes = [i32, i32, i32]
+    L.vg_accept_workspace_size.restype = sz
+    L.vg_accept.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, u32, vp, vp, vp, vp, sz, vp, vp]
+    L.vg_accept.restype = i32
     L.vg_sparse_draft_launches.argtypes = [ctypes.POINTER(vg_dims), i32, i32]
     L.vg_sparse_draft_launches.restype = i32
     L.vg_last_error.argtypes = []
@@ -173,6 +178,26 @@ def vg_topk_select(scores, score_stride, len_, B, max_len, k, idx, count, ws=Non
 def vg_window_select(len_, B, max_len, k, idx, count, dev_status=None, stream=None) -> None:
     """The last min(k, len) positions of each sequence (the sliding-window baseline)."""
     _check(load().vg_window_select(ptr(len_), B, max_len, k, ptr(idx), ptr(count), ptr(dev_status), _stream(stream)))
+
+
+VG_ACCEPT_GREEDY = 0
+VG_ACCEPT_SAMPLE = 1
+
+
+def vg_accept_workspace_size(B: int, gamma: int, V: int) -> int:
+    n = load().vg_accept_workspace_size(B, gamma, V)
+    if n == 0:
+        raise VgError(VG_ERR_UNSUPPORTED_SHAPE, load().vg_last_error().decode())
+    return n
+
+
+def vg_accept(B, gamma, V, p_logits, q_logits, draft_tokens, u_accept, u_resample, mode, n_accept, next_token,
+              advance_len, ws, ws_bytes=None, dev_status=None, stream=None) -> None:
+    """Acceptance of the draft chain (greedy or speculative sampling) on given logits."""
+    wsb = ws_bytes if ws_bytes is not None else (ws.numel() * ws.element_size() if ws is not None else 0)
+    _check(load().vg_accept(B, gamma, V, ptr(p_logits), ptr(q_logits), ptr(draft_tokens), ptr(u_accept),
+                            ptr(u_resample), mode, ptr(n_accept), ptr(next_token), ptr(advance_len), ptr(ws), wsb,
+                            ptr(dev_status), _stream(stream)))
 
 
 VG_DRAFT_SELECTION_SETTLED = 1

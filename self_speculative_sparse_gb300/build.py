@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libvg.so")
 
-SOURCES = ["vg_api.cu", "verify_attn.cu", "topk_select.cu", "sparse_draft.cu"]
+SOURCES = ["vg_api.cu", "verify_attn.cu", "topk_select.cu", "sparse_draft.cu", "accept.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

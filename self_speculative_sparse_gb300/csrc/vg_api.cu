@@ -606,6 +606,56 @@ vg_status vg_topk_select(const float* scores, int64_t score_stride, const int32_
                   static_cast<cudaStream_t>(stream), true);
 }
 
+size_t vg_accept_workspace_size(int32_t B, int32_t gamma, int32_t V) {
+  g_err.clear();
+  if (B < 1 || B > kMaxBatch || gamma < 0 || gamma > 15 || V < 1 || V > kMaxAcceptTiles * 4096) {
+    fail(VG_ERR_UNSUPPORTED_SHAPE, "B=%d, gamma=%d or V=%d out of range", B, gamma, V);
+    return 0;
+  }
+  const size_t rows = static_cast<size_t>(B) * (2 * gamma + 1);
+  return up256(rows * accept_chunks(V) * 16);
+}
+
+vg_status vg_accept(int32_t B, int32_t gamma, int32_t V, const float* p_logits, const float* q_logits,
+                    const int32_t* draft_tokens, const float* u_accept, const float* u_resample, uint32_t mode,
+                    int32_t* n_accept, int32_t* next_token, int32_t* advance_len, void* ws, size_t ws_bytes,
+                    int32_t* dev_status, void* stream) {
+  g_err.clear();
+  if (mode != VG_ACCEPT_GREEDY && mode != VG_ACCEPT_SAMPLE) return fail(VG_ERR_INVALID_ARG, "mode=%u unknown", mode);
+  const bool sample = mode == VG_ACCEPT_SAMPLE;
+  const size_t need = vg_accept_workspace_size(B, gamma, V);
+  if (need == 0) return VG_ERR_UNSUPPORTED_SHAPE;
+  if (!p_logits || !n_accept || !next_token || (gamma > 0 && !draft_tokens))
+    return fail(VG_ERR_INVALID_ARG, "p_logits, draft_tokens, n_accept and next_token must be non-NULL");
+  if (sample && (!u_resample || (gamma > 0 && (!q_logits || !u_accept))))
+    return fail(VG_ERR_INVALID_ARG, "sampling needs q_logits, u_accept and u_resample");
+  if (!aligned16(p_logits) || !aligned16(q_logits) || !aligned16(draft_tokens) || !aligned16(u_accept) ||
+      !aligned16(u_resample) || !aligned16(n_accept) || !aligned16(next_token) || !aligned16(advance_len))
+    return fail(VG_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0) return fail(VG_ERR_INVALID_ARG, "dev_status must be 4-byte aligned");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < need)
+    return fail(VG_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", need);
+  AcceptParams p = {};
+  p.p_logits = p_logits;
+  p.q_logits = q_logits;
+  p.draft = draft_tokens;
+  p.u = u_accept;
+  p.u_res = u_resample;
+  p.B = B;
+  p.gamma = gamma;
+  p.V = V;
+  p.nchunk = accept_chunks(V);
+  p.sample = sample ? 1 : 0;
+  p.stats = static_cast<float*>(ws);
+  p.n_accept = n_accept;
+  p.next_token = next_token;
+  p.advance_len = advance_len;
+  p.status = dev_status;
+  const cudaError_t e = launch_accept(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "accept launch");
+  return VG_OK;
+}
+
 vg_status vg_window_select(const int32_t* len, int32_t B, int32_t max_len, int32_t k, int32_t* idx, int32_t* count,
                            int32_t* dev_status, void* stream) {
   g_err.clear();

@@ -87,6 +87,23 @@ struct DraftParams {
   int32_t* status;
 };
 
+// Most 4096-entry tiles of the vocabulary the acceptance step draws from (V <= 2^20).
+constexpr int kMaxAcceptTiles = 256;
+
+struct AcceptParams {
+  const float* p_logits;   // [B][gamma+1][V]
+  const float* q_logits;   // [B][gamma][V] (sampling only)
+  const int32_t* draft;    // [B][gamma]
+  const float* u;          // [B][gamma] (sampling only)
+  const float* u_res;      // [B] (sampling only)
+  int B, gamma, V, nchunk, sample;
+  float* stats;            // [rows][nchunk] (max, sum, argmax value, argmax) per chunk
+  int32_t* n_accept;       // [B]
+  int32_t* next_token;     // [B]
+  int32_t* advance_len;    // [B] or null
+  int32_t* status;
+};
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream);
@@ -102,6 +119,8 @@ cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t
                           int32_t* status, cudaStream_t stream);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
 size_t draft_smem_bytes(int D, int Hkv);
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
+int accept_chunks(int V);  // vocabulary chunks of the statistics kernel
 // Warps of the draft step's combine kernel (4, 8 or 16 from the most partials a
 // sequence has), or 0 when every sequence's entries sit in one CTA (no combine runs).
 int draft_combine_warps(int B, int slots, int nctas);

@@ -299,6 +299,24 @@ WORKLOADS = {
 }
 
 
+# ---------------------------------------------------------------- acceptance inputs
+def accept_inputs(B: int, gamma: int, V: int, seed: int, scale: float = 3.0, noise: float = 1.0) -> dict:
+    """Synthetic inputs of the acceptance step (fp32 logits, as a model's output head
+    gives them): target logits p [B][gamma+1][V] = scale * N(0,1); draft logits
+    q [B][gamma][V] = p[:, :gamma] + noise * N(0,1) (a draft close to the target); draft
+    tokens x [B][gamma] drawn from the draft's distribution by the Gumbel-max trick
+    (argmax of q plus Gumbel noise, which samples softmax(q) without computing it);
+    uniforms u [B][gamma] and u_res [B] in [0, 1).  numpy's seeded generator."""
+    r = np.random.default_rng(seed)
+    p = (scale * r.standard_normal((B, gamma + 1, V))).astype(np.float32)
+    q = (p[:, :gamma] + noise * r.standard_normal((B, gamma, V))).astype(np.float32)
+    gumbel = -np.log(-np.log(r.uniform(1e-12, 1.0, size=(B, gamma, V))))
+    x = np.argmax(q.astype(np.float64) + gumbel, axis=-1).astype(np.int32) if gamma else np.zeros((B, 0), np.int32)
+    u = r.uniform(0.0, 1.0, size=(B, gamma)).astype(np.float32)
+    u_res = r.uniform(0.0, 1.0, size=B).astype(np.float32)
+    return dict(p_logits=p, q_logits=q, x=x, u=u, u_res=u_res)
+
+
 def scaled(w: Workload, **kw) -> Workload:
     """A copy of a workload with some fields replaced (small parity cases)."""
     from dataclasses import replace
