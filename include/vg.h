@@ -85,12 +85,28 @@ typedef struct vg_dims {
   float scale;     /* logit scale; 0 means 1/sqrt(d)                                  */
 } vg_dims;
 
-/* The KV cache of one layer (host struct holding device pointers). */
+/* The KV cache of one layer (host struct holding device pointers).
+ *
+ * Two layouts of the same slot pool (one slot = one token's keys of every KV head):
+ *   page_table == NULL: sequence b's token i lives in slot seq_offset[b] + i;
+ *   page_table != NULL: the vLLM-style block table of Vegas §3 (the draft runs as a
+ *     paged attention whose pages are tokens): the pool is cut into pages of page_size
+ *     slots (page p = slots p * page_size .. p * page_size + page_size - 1) and token i
+ *     of sequence b lives in row i % page_size of page page_table[b][i / page_size].
+ *     seq_offset is then unused (may be NULL).  Page entries outside the pool are
+ *     reported on the device as VG_ERR_DEVICE_BOUNDS and their tokens skipped.
+ *     vg_sparse_draft_attn reads any page_size >= 1; vg_verify_attn and vg_iteration
+ *     need page_size 8, 16, 32 or a multiple of 64 (VG_ERR_UNSUPPORTED_SHAPE otherwise).
+ *     pages_per_seq (>= 1) is the row stride of page_table; a sequence's prefix plus
+ *     its gamma+1 verify rows must fit pages_per_seq * page_size tokens. */
 typedef struct vg_kv_cache {
   void* K;                    /* bf16 [capacity_slots][H_kv][d]                       */
   void* V;                    /* bf16 [capacity_slots][H_kv][d]                       */
   const int64_t* seq_offset;  /* device int64 [B]: slot of token 0 of sequence b      */
   int64_t capacity_slots;     /* slots in K and V                                     */
+  const int32_t* page_table;  /* device int32 [B][pages_per_seq], or NULL             */
+  int32_t page_size;          /* tokens per page (page_table only)                    */
+  int32_t pages_per_seq;      /* row stride of page_table (page_table only)          */
 } vg_kv_cache;
 
 /*

@@ -27,4 +27,5 @@ from .vegas import (  # noqa: F401
     accept_greedy,
     accept_sample,
     next_prefix_len,
+    paged_slots,
 )

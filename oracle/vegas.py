@@ -182,6 +182,16 @@ def selection_overlap(a: np.ndarray, b: np.ndarray, k: int) -> float:
     return len(np.intersect1d(a, b)) / float(k)
 
 
+# ------------------------------------------------------------------ paged cache
+def paged_slots(table_row: np.ndarray, page_size: int, n: int) -> np.ndarray:
+    """Physical slots of tokens 0..n-1 of one sequence in a paged cache (the block table
+    of Vegas §3, whose draft kernel takes tokens as pages): token i lives in row
+    i % page_size of page table_row[i // page_size], page p holding slots
+    p * page_size .. p * page_size + page_size - 1.  int64 [n]."""
+    i = np.arange(n, dtype=np.int64)
+    return np.asarray(table_row, dtype=np.int64)[i // page_size] * page_size + i % page_size
+
+
 # ------------------------------------------------------------------ drafting
 def sparse_draft_attention(q: np.ndarray, K_sel: np.ndarray, V_sel: np.ndarray,
                            scale: float | None = None) -> np.ndarray:

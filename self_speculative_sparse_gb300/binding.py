@@ -43,7 +43,8 @@ class vg_dims(ctypes.Structure):
 
 class vg_kv_cache(ctypes.Structure):
     _fields_ = [("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("seq_offset", ctypes.c_void_p),
-                ("capacity_slots", ctypes.c_int64)]
+                ("capacity_slots", ctypes.c_int64), ("page_table", ctypes.c_void_p), ("page_size", ctypes.c_int32),
+                ("pages_per_seq", ctypes.c_int32)]
 
 
 class vg_iter_inputs(ctypes.Structure):
@@ -141,9 +142,13 @@ def make_dims(B, H_q, H_kv, d, gamma, max_len, scale=0.0) -> vg_dims:
     return vg_dims(B, H_q, H_kv, d, gamma, max_len, scale)
 
 
-def make_cache(K, V, seq_offset, capacity_slots: int | None = None) -> vg_kv_cache:
+def make_cache(K, V, seq_offset, capacity_slots: int | None = None, page_table=None, page_size: int = 0) -> vg_kv_cache:
+    """The cache struct: a slot pool located by seq_offset, or pages through page_table
+    (int32 [B][pages_per_seq] tensor)."""
     cap = capacity_slots if capacity_slots is not None else K.shape[0]
-    return vg_kv_cache(ptr(K), ptr(V), ptr(seq_offset), cap)
+    if page_table is None:
+        return vg_kv_cache(ptr(K), ptr(V), ptr(seq_offset), cap, None, 0, 0)
+    return vg_kv_cache(ptr(K), ptr(V), ptr(seq_offset), cap, ptr(page_table), page_size, page_table.shape[1])
 
 
 def vg_sparse_draft_launches(dims: vg_dims, k_stride: int, tail_len_max: int = 0) -> int:

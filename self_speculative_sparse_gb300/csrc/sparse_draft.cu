@@ -64,11 +64,12 @@ __device__ __forceinline__ int tail_len_of(const DraftParams& p, int b) {
 // faulted, if out of range).
 template <int D>
 __device__ __forceinline__ void append_token(const DraftParams& p, int b, int g, int t, int nt) {
-  const int64_t off = p.seq_offset[b];
   const int ts = p.tail_start[b];
   const int tl = tail_len_of(p, b);
-  if (!(off >= 0 && ts >= 0 && tl >= 1 && tl <= kDraftMaxTail && off + ts + tl <= p.capacity)) return;
-  const size_t dst = ((off + ts + tl - 1) * p.Hkv + g) * D;
+  if (!(ts >= 0 && tl >= 1 && tl <= kDraftMaxTail)) return;
+  const int64_t slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, ts + tl - 1);
+  if (slot < 0) return;
+  const size_t dst = (slot * p.Hkv + g) * D;
   const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
   for (int c = t; c < D / 8; c += nt) {
     reinterpret_cast<uint4*>(p.K + dst)[c] = reinterpret_cast<const uint4*>(p.k_new + src)[c];
@@ -103,10 +104,9 @@ __device__ __forceinline__ ChunkPos resolve(const DraftParams& p, int b, int j, 
   const int cnt_raw = __ldcg(p.count + b);
   const int tl = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
   const int ts = __ldcg(p.tail_start + b);
-  const int64_t off = __ldcg(p.seq_offset + b);
   const int sel = (lane < nvalid && jj < p.k_stride) ? __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj) : 0;
   const bool seq_ok = cnt_raw >= 0 && cnt_raw <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && cnt_raw + tl <= S &&
-                      off >= 0 && ts >= 0 && off + ts + tl <= p.capacity && (p.k_new == nullptr || tl >= 1);
+                      ts >= 0 && (p.k_new == nullptr || tl >= 1);
   if (!seq_ok && lane == 0 && j == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
   const int nsel = seq_ok ? cnt_raw : 0;
   ChunkPos c{-1, false, nullptr, nullptr};
@@ -127,8 +127,14 @@ __device__ __forceinline__ ChunkPos resolve(const DraftParams& p, int b, int j, 
       c.ksrc = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
       c.vsrc = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
     } else {
-      c.ksrc = p.K + static_cast<size_t>(off + c.pos) * p.Hkv * D;
-      c.vsrc = p.V + static_cast<size_t>(off + c.pos) * p.Hkv * D;
+      const int64_t slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, c.pos);
+      if (slot < 0) {  // outside the cache (or the page table): skipped, reported
+        report(p.status, VG_ERR_DEVICE_BOUNDS);
+        c.pos = -1;
+      } else {
+        c.ksrc = p.K + static_cast<size_t>(slot) * p.Hkv * D;
+        c.vsrc = p.V + static_cast<size_t>(slot) * p.Hkv * D;
+      }
     }
   }
   return c;
@@ -380,14 +386,15 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   int64_t adst = -1;
   if (app) {
     const int g = h / p.G;
-    const int64_t off = p.seq_offset[b];
     const int ts = p.tail_start[b];
     const int tl = tail_len_of(p, b);
     const size_t src = (static_cast<size_t>(b) * p.Hkv + g) * D;
     kr = reinterpret_cast<const uint4*>(p.k_new + src)[tid];
     vr = reinterpret_cast<const uint4*>(p.v_new + src)[tid];
-    if (off >= 0 && ts >= 0 && tl >= 1 && tl <= kDraftMaxTail && off + ts + tl <= p.capacity)
-      adst = ((off + ts + tl - 1) * p.Hkv + g) * D;
+    if (ts >= 0 && tl >= 1 && tl <= kDraftMaxTail) {
+      const int64_t slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, ts + tl - 1);
+      if (slot >= 0) adst = (slot * p.Hkv + g) * D;
+    }
   }
   // The next draft step may start once the draft kernel before this one completed: a
   // step with a settled selection gathers before its own dependency wait, which is

@@ -94,6 +94,27 @@ static_assert(TCfg<64, 64>::smem(kMaxBatch) <= 232448 && TCfg<64, 128>::smem(kMa
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// A prefix length the cache can hold with the gamma+1 verify rows after it: the slot
+// pool from seq_offset[b] on, or the sequence's pages in the page table (page entries
+// are checked where they are read).
+__device__ __forceinline__ bool seq_len_ok(const VerifyParams& p, int b, int n) {
+  if (n < 0 || n > p.max_len) return false;
+  if (p.ptab) return static_cast<int64_t>(n) + p.R <= static_cast<int64_t>(p.pstride) * p.psize;
+  const int64_t off = p.seq_offset[b];
+  return off >= 0 && off + static_cast<int64_t>(n) + p.R <= p.capacity;
+}
+
+// The key / value row of verify row u of sequence b (prefix length n), KV head g: from
+// the inputs when given, else from the cache slot after the prefix (null if that slot
+// is outside the cache).
+template <int D>
+__device__ __forceinline__ const __nv_bfloat16* verify_row(const VerifyParams& p, const __nv_bfloat16* fresh,
+                                                           const __nv_bfloat16* cache, int b, int n, int u, int g) {
+  if (fresh) return fresh + ((static_cast<size_t>(b) * p.R + u) * p.Hkv + g) * D;
+  const int64_t slot = kv_slot(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, n + u);
+  return slot >= 0 ? cache + (slot * p.Hkv + g) * D : nullptr;
+}
+
 // Per-sequence tile counts (one KV head) and checked lengths; warp 0 only.
 // nlen[b] = -1 marks a sequence whose length or slots are out of range.
 __device__ void seq_meta(const VerifyParams& p, int* cum, int* nlen) {
@@ -104,9 +125,7 @@ __device__ void seq_meta(const VerifyParams& p, int* cum, int* nlen) {
     int tiles = 0;
     if (b < p.B) {
       int n = p.prefix_len[b];
-      const int64_t off = p.seq_offset[b];
-      const bool ok = n >= 0 && n <= p.max_len && off >= 0 && off + (int64_t)n + p.R <= p.capacity;
-      if (!ok) {
+      if (!seq_len_ok(p, b, n)) {
         report(p.status, VG_ERR_DEVICE_BOUNDS);
         n = -1;
       }
@@ -156,7 +175,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_
   return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, status, abort));
 }
 
-template <int D, int MR>
+// PAGED: the cache is read through a page table (a separate instantiation, so that the
+// slot pool's kernel keeps its lean producer).
+template <int D, int MR, bool PAGED>
 __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     verify_kernel(const VerifyParams p, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
@@ -245,34 +266,122 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
   const int t0 = static_cast<int>(split_begin(blockIdx.x, T, p.nctas));
   const int ntiles = static_cast<int>(split_begin(blockIdx.x + 1, T, p.nctas)) - t0;
 
-  if (ntiles > 0 && warp == C::RWARPS && lane == 0) {
-    // ---------------------------------------------------------------- TMA producer
+  if (!PAGED && ntiles > 0 && warp == C::RWARPS) {
+    // ---------------------------------------------------------------- TMA producer (slot pool)
+    // one thread: a tile of 64 keys is one box per half of K and of V
+    if (lane == 0) {
+      int b, g, j;
+      locate(t0, cum, p.B, p.Hkv, b, g, j);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % S;
+        // after the first stage, the first run's query rows go first: issued together
+        // with the whole ring, their loads would queue behind it (about 3 us at the start)
+        if (i == 1 && !mbar_wait_ab(q_landed, 0, p.status, abort)) break;
+        if (i >= S && !mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort)) break;
+        fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
+        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        uint8_t* kdst = smem + st * C::STAGE_BYTES;
+        uint8_t* vdst = kdst + C::TILE_BYTES;
+        const int y = static_cast<int>(p.seq_offset[b] + static_cast<int64_t>(j) * TK);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, g * D + h * 64, y, &full[st]);
+          tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, g * D + h * 64, y, &full[st]);
+        }
+        ++issued;
+        advance(b, g, j, cum, p.B, p.Hkv);
+      }
+      // no copy may still be in flight when the CTA exits (normally all were consumed)
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
+    }
+    __syncwarp();
+  } else if (PAGED && ntiles > 0 && warp == C::RWARPS) {
+    // ---------------------------------------------------------------- TMA producer (paged)
+    // A tile of 64 keys is 64 / box_rows boxes, each at its page's physical rows; lane s
+    // issues boxes s and s + 32.  Boxes wholly past the prefix are not loaded (their rows
+    // are masked, and the row warps zero such value rows).  Lane 0 takes the waits and
+    // the byte count.
     int b, g, j;
     locate(t0, cum, p.B, p.Hkv, b, g, j);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int BR = p.box_rows;
+    // Row of box s of tile (b, j) for the lane's two boxes (-1: no box), looked up one
+    // tile ahead so that the table's loads overlap the wait for the ring.
+    auto lookup = [&](int bb, int jj, int (&y)[2]) {
+      const int keys = min(TK, nlen[bb] - jj * TK);  // keys of the tile inside the prefix (> 0)
+      const int nbox = (keys + BR - 1) / BR;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int s_ = lane + 32 * k;
+        y[k] = -1;
+        if (s_ >= nbox) continue;
+        const int64_t slot =
+            kv_slot(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, bb, static_cast<int64_t>(jj) * TK + s_ * BR);
+        if (slot < 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
+        y[k] = static_cast<int>(slot);
+      }
+    };
+    // rows of tiles i .. i + LA - 1 (a ring of lookups, LA tiles ahead of the copies)
+    constexpr int LA = 4;
+    int yq[LA][2];
+    int bl = b, gl = g, jl = j;  // the lookup cursor
+    for (int i = 0; i < LA && i < ntiles; ++i) {
+      lookup(bl, jl, yq[i]);
+      advance(bl, gl, jl, cum, p.B, p.Hkv);
+    }
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % S;
+      int ycur[2] = {yq[i % LA][0], yq[i % LA][1]};
+      // the rows of tile i + LA, while this tile waits for its stage
+      if (i + LA < ntiles) {
+        lookup(bl, jl, yq[i % LA]);
+        advance(bl, gl, jl, cum, p.B, p.Hkv);
+      }
+      int bn = b, gn = g, jn = j;
+      advance(bn, gn, jn, cum, p.B, p.Hkv);
       // after the first stage, the first run's query rows go first: issued together
       // with the whole ring, their loads would queue behind it (about 3 us at the start)
-      if (i == 1 && !mbar_wait_ab(q_landed, 0, p.status, abort)) break;
-      if (i >= S && !mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort)) break;
-      fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
-      mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+      bool ok = true;
+      if (lane == 0) {
+        if (i == 1) ok = mbar_wait_ab(q_landed, 0, p.status, abort);
+        if (ok && i >= S) ok = mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int nload = __popc(__ballot_sync(0xffffffffu, ycur[0] >= 0)) + __popc(__ballot_sync(0xffffffffu, ycur[1] >= 0));
+      if (lane == 0) {
+        fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nload * BR * 128 * C::HALVES * 2));
+      }
+      __syncwarp();
       uint8_t* kdst = smem + st * C::STAGE_BYTES;
       uint8_t* vdst = kdst + C::TILE_BYTES;
-      const int y = static_cast<int>(p.seq_offset[b] + static_cast<int64_t>(j) * TK);
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, g * D + h * 64, y, &full[st]);
-        tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, g * D + h * 64, y, &full[st]);
+      for (int k = 0; k < 2; ++k) {
+        if (ycur[k] >= 0) {
+          const int off = (lane + 32 * k) * BR * 128;
+#pragma unroll
+          for (int h = 0; h < C::HALVES; ++h) {
+            tma_load_2d(kdst + h * C::HALF_BYTES + off, &tmK, g * D + h * 64, ycur[k], &full[st]);
+            tma_load_2d(vdst + h * C::HALF_BYTES + off, &tmV, g * D + h * 64, ycur[k], &full[st]);
+          }
+        }
       }
       ++issued;
-      advance(b, g, j, cum, p.B, p.Hkv);
+      b = bn;
+      g = gn;
+      j = jn;
     }
     // no copy may still be in flight when the CTA exits (normally all were consumed)
-    for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
+    if (lane == 0)
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1, p.status);
+    __syncwarp();
   } else if (ntiles > 0 && warp == C::RWARPS + 1 && lane == 0) {
     // ---------------------------------------------------------------- Q K^T issuer
     constexpr uint32_t idS = tc_idesc_bf16(MR, TK, 0, 0);
@@ -619,12 +728,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
     const bool active = r < p.M;
     const int t = active ? r / G : 0, jh = r - t * G;
     const int tmax = min(p.M - 1, r0 + kCombineWarps - 1) / G;  // last verify row of this CTA
-    const int64_t base = p.seq_offset[b];
-    const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
-    const __nv_bfloat16* kn = p.k_new ? p.k_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
-                                      : p.K + ((base + n) * p.Hkv + g) * D;
-    const __nv_bfloat16* vn = p.v_new ? p.v_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
-                                      : p.V + ((base + n) * p.Hkv + g) * D;
     // partials of this (sequence, KV head): CTAs cf..cl of the verify split
     const int tiles = cum[b + 1] - cum[b];
     const int64_t T = static_cast<int64_t>(p.Hkv) * cum[p.B];
@@ -668,8 +771,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
     for (int e = tid; e < 2 * (tmax + 1) * CH; e += kCombineWarps * 32) {
       const int which = e / ((tmax + 1) * CH), rem = e - which * (tmax + 1) * CH;
       const int u = rem / CH, c = rem - u * CH;
+      const __nv_bfloat16* row = which ? verify_row<D>(p, p.v_new, p.V, b, n, u, g) : verify_row<D>(p, p.k_new, p.K, b, n, u, g);
       reinterpret_cast<uint4*>(&kvs[which][u][0])[c] =
-          reinterpret_cast<const uint4*>((which ? vn : kn) + u * row_stride)[c];
+          row ? reinterpret_cast<const uint4*>(row)[c] : make_uint4(0u, 0u, 0u, 0u);
     }
     float pm = NEG, pl = 0.f;
     float va[NB][PER], vb[NB][PER];
@@ -749,11 +853,14 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2) verify_combine_kernel(c
 #pragma unroll
     for (int e = 0; e < PER; ++e) o[e] = __float2bfloat16_rn(acc[e] * inv);
     if (p.k_new && jh == 0) {  // append verify row t (the chain enters the cache)
-      const size_t dst = ((base + n + t) * p.Hkv + g) * D + lane * PER;
+      const int64_t slot = kv_slot(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, n + t);
+      if (slot >= 0) {
+        const size_t dst = (slot * p.Hkv + g) * D + lane * PER;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        p.K[dst + e] = kvs[0][t][lane * PER + e];
-        p.V[dst + e] = kvs[1][t][lane * PER + e];
+        for (int e = 0; e < PER; ++e) {
+          p.K[dst + e] = kvs[0][t][lane * PER + e];
+          p.V[dst + e] = kvs[1][t][lane * PER + e];
+        }
       }
     }
     return;
@@ -819,8 +926,7 @@ __device__ void combine_seq_meta(const VerifyParams& p, int b, int* out4) {
     int tiles = 0, n = -1;
     if (bb < p.B) {
       n = p.prefix_len[bb];
-      const int64_t off = p.seq_offset[bb];
-      if (!(n >= 0 && n <= p.max_len && off >= 0 && off + (int64_t)n + p.R <= p.capacity)) n = -1;
+      if (!seq_len_ok(p, bb, n)) n = -1;
       tiles = n > 0 ? (n + TK - 1) / TK : 0;
     }
     int tb = bb < b ? tiles : 0;
@@ -875,18 +981,13 @@ __global__ void __launch_bounds__(kNarrowThreads, 4) verify_combine_narrow_kerne
     __syncthreads();
     const int n = smeta[3];
     if (n < 0) return;  // the whole CTA
-    const int64_t base = p.seq_offset[b];
-    const size_t row_stride = static_cast<size_t>(p.Hkv) * D;  // between consecutive verify rows
-    const __nv_bfloat16* kn = p.k_new ? p.k_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
-                                      : p.K + ((base + n) * p.Hkv + g) * D;
-    const __nv_bfloat16* vn = p.v_new ? p.v_new + (static_cast<size_t>(b) * p.R * p.Hkv + g) * D
-                                      : p.V + ((base + n) * p.Hkv + g) * D;
     constexpr int CH = D / 8;  // 16-byte chunks of a row
     for (int e = tid; e < 2 * (tmax + 1) * CH; e += kNarrowThreads) {
       const int which = e / ((tmax + 1) * CH), rem = e - which * (tmax + 1) * CH;
       const int u = rem / CH, c = rem - u * CH;
+      const __nv_bfloat16* row = which ? verify_row<D>(p, p.v_new, p.V, b, n, u, g) : verify_row<D>(p, p.k_new, p.K, b, n, u, g);
       reinterpret_cast<uint4*>(&skv[which][u][0])[c] =
-          reinterpret_cast<const uint4*>((which ? vn : kn) + u * row_stride)[c];
+          row ? reinterpret_cast<const uint4*>(row)[c] : make_uint4(0u, 0u, 0u, 0u);
     }
     for (int e = tid; e < RPC * CH; e += kNarrowThreads) {
       const int rr = e / CH, c = e - rr * CH;
@@ -978,9 +1079,12 @@ __global__ void __launch_bounds__(kNarrowThreads, 4) verify_combine_narrow_kerne
     }
     p.out[((static_cast<size_t>(b) * p.R + t) * p.Hq + g * G + jh) * D + d] = __float2bfloat16_rn(acc / lr);
     if (p.k_new && jh == 0) {  // append verify row t (the chain enters the cache)
-      const size_t dst = ((base + n + t) * p.Hkv + g) * D + d;
-      p.K[dst] = skv[0][t][d];
-      p.V[dst] = skv[1][t][d];
+      const int64_t slot = kv_slot(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, n + t);
+      if (slot >= 0) {
+        const size_t dst = (slot * p.Hkv + g) * D + d;
+        p.K[dst] = skv[0][t][d];
+        p.V[dst] = skv[1][t][d];
+      }
     }
     return;
   }
@@ -992,10 +1096,7 @@ __global__ void __launch_bounds__(kNarrowThreads, 4) verify_combine_narrow_kerne
   const int b = sb / nchunks, ch = sb - b * nchunks;
   if (b >= p.B) return;
   const int n = p.prefix_len[b];
-  {
-    const int64_t off = p.seq_offset[b];
-    if (!(n >= 0 && n <= p.max_len && off >= 0 && off + (int64_t)n + p.R <= p.capacity)) return;
-  }
+  if (!seq_len_ok(p, b, n)) return;
   const int pos = ch * CHS + tid * 2;
   if (pos >= n) return;
   pdl_wait();
@@ -1023,12 +1124,12 @@ __global__ void __launch_bounds__(kNarrowThreads, 4) verify_combine_narrow_kerne
   }
 }
 
-template <int D, int MR>
+template <int D, int MR, bool PAGED>
 cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                             cudaStream_t stream) {
   using C = TCfg<D, MR>;
   const size_t smem = C::smem(p.B);
-  cudaError_t e = ensure_smem<verify_kernel<D, MR>>(smem);
+  cudaError_t e = ensure_smem<verify_kernel<D, MR, PAGED>>(smem);
   if (e != cudaSuccess) return e;
   {
     cudaLaunchAttribute at[1];
@@ -1041,11 +1142,11 @@ cudaError_t launch_verify_t(const VerifyParams& p, const CUtensorMap& tmK, const
     cfg.stream = stream;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, verify_kernel<D, MR>, p, tmK, tmV);
+    e = cudaLaunchKernelEx(&cfg, verify_kernel<D, MR, PAGED>, p, tmK, tmV);
   }
   if (e != cudaSuccess) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, verify_kernel<D, MR>) == cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, verify_kernel<D, MR, PAGED>) == cudaSuccess) {
       fprintf(stderr,
               "verify_kernel<%d,%d>: %s (regs=%d maxThreads=%d threads=%d staticSmem=%zu maxDynSmem=%d "
               "requestedSmem=%zu localBytes=%zu)\n",
@@ -1103,12 +1204,17 @@ cudaError_t launch_verify(const VerifyParams& p, const CUtensorMap& tmK, const C
   // A-operand rows: the query rows, then a high and a low row per score mask
   const int nsc = 2 * ((p.mask0 ? 1 : 0) + (p.mask1 ? 1 : 0));
   const int arows = nsc ? p.sc_row0 + nsc : p.M;
+  const bool paged = p.ptab != nullptr;
   if (arows <= 64) {
-    if (p.D == 64) return launch_verify_t<64, 64>(p, tmK, tmV, stream);
-    if (p.D == 128) return launch_verify_t<128, 64>(p, tmK, tmV, stream);
+    if (p.D == 64) return paged ? launch_verify_t<64, 64, true>(p, tmK, tmV, stream)
+                                : launch_verify_t<64, 64, false>(p, tmK, tmV, stream);
+    if (p.D == 128) return paged ? launch_verify_t<128, 64, true>(p, tmK, tmV, stream)
+                                 : launch_verify_t<128, 64, false>(p, tmK, tmV, stream);
   } else {
-    if (p.D == 64) return launch_verify_t<64, 128>(p, tmK, tmV, stream);
-    if (p.D == 128) return launch_verify_t<128, 128>(p, tmK, tmV, stream);
+    if (p.D == 64) return paged ? launch_verify_t<64, 128, true>(p, tmK, tmV, stream)
+                                : launch_verify_t<64, 128, false>(p, tmK, tmV, stream);
+    if (p.D == 128) return paged ? launch_verify_t<128, 128, true>(p, tmK, tmV, stream)
+                                 : launch_verify_t<128, 128, false>(p, tmK, tmV, stream);
   }
   return cudaErrorInvalidValue;
 }

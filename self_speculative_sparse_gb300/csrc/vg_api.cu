@@ -86,14 +86,15 @@ vg_status get_encoder(EncodeTiledFn* fn) {
   return VG_OK;
 }
 
-// [capacity][Hkv*D] bf16 viewed as a 2-D tensor; boxes of 64 columns x 64 rows, 128-byte swizzle.
-vg_status encode_cache_map(CUtensorMap* map, void* base, int64_t capacity, int Hkv, int D) {
+// [capacity][Hkv*D] bf16 viewed as a 2-D tensor; boxes of 64 columns x box_rows rows
+// (64 for the slot pool, the page's rows for a paged cache), 128-byte swizzle.
+vg_status encode_cache_map(CUtensorMap* map, void* base, int64_t capacity, int Hkv, int D, int box_rows) {
   EncodeTiledFn enc;
   vg_status st = get_encoder(&enc);
   if (st != VG_OK) return st;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hkv) * D, static_cast<cuuint64_t>(capacity)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hkv) * D * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kVerifyTileKeys)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -138,12 +139,32 @@ vg_status check_dims(const vg_dims* d, Shape* s) {
 
 vg_status check_cache(const vg_kv_cache* c) {
   if (!c) return fail(VG_ERR_INVALID_ARG, "cache is NULL");
-  if (!c->K || !c->V || !c->seq_offset) return fail(VG_ERR_INVALID_ARG, "cache K, V and seq_offset must be non-NULL");
-  if (!aligned16(c->K) || !aligned16(c->V) || !aligned16(c->seq_offset))
+  if (!c->K || !c->V) return fail(VG_ERR_INVALID_ARG, "cache K and V must be non-NULL");
+  if (!c->page_table && !c->seq_offset) return fail(VG_ERR_INVALID_ARG, "seq_offset must be non-NULL without a page table");
+  if (!aligned16(c->K) || !aligned16(c->V) || !aligned16(c->seq_offset) || !aligned16(c->page_table))
     return fail(VG_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
   if (c->capacity_slots < 1 || c->capacity_slots > 0x7fffffffLL)
     return fail(VG_ERR_INVALID_ARG, "capacity_slots=%lld outside [1, 2^31)", static_cast<long long>(c->capacity_slots));
+  if (c->page_table) {
+    if (c->page_size < 1 || c->page_size > (1 << 20) || c->page_size > c->capacity_slots)
+      return fail(VG_ERR_INVALID_ARG, "page_size=%d outside [1, min(2^20, capacity_slots)]", c->page_size);
+    if (c->pages_per_seq < 1) return fail(VG_ERR_INVALID_ARG, "pages_per_seq=%d < 1", c->pages_per_seq);
+  }
   return VG_OK;
+}
+
+// The verify pass reads a paged cache as TMA boxes of a page's rows, which keeps each
+// box's shared-memory destination on the swizzle pattern's 1024-byte period for pages of
+// 8, 16 or 32 tokens or a multiple of 64; the draft step reads any page size.
+vg_status check_verify_pages(const vg_kv_cache* c) {
+  if (!c->page_table) return VG_OK;
+  const int P = c->page_size;
+  if (P == 8 || P == 16 || P == 32 || P % 64 == 0) return VG_OK;
+  return fail(VG_ERR_UNSUPPORTED_SHAPE, "verify reads pages of 8, 16, 32 or a multiple of 64 tokens (page_size=%d)", P);
+}
+
+int verify_box_rows(const vg_kv_cache* c) {
+  return c->page_table ? (c->page_size < kVerifyTileKeys ? c->page_size : kVerifyTileKeys) : kVerifyTileKeys;
 }
 
 vg_status check_mask(uint32_t mask, int R, const char* name) {
@@ -239,9 +260,9 @@ vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, 
   if (verify_smem_bytes(s.D, s.B) > di.smem_optin)
     return fail(VG_ERR_UNSUPPORTED_SHAPE, "verify needs %zu bytes of shared memory", verify_smem_bytes(s.D, s.B));
   CUtensorMap tmK, tmV;
-  vg_status st = encode_cache_map(&tmK, c->K, c->capacity_slots, s.Hkv, s.D);
+  vg_status st = encode_cache_map(&tmK, c->K, c->capacity_slots, s.Hkv, s.D, verify_box_rows(c));
   if (st != VG_OK) return st;
-  st = encode_cache_map(&tmV, c->V, c->capacity_slots, s.Hkv, s.D);
+  st = encode_cache_map(&tmV, c->V, c->capacity_slots, s.Hkv, s.D, verify_box_rows(c));
   if (st != VG_OK) return st;
   VerifyParams p = {};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -250,6 +271,10 @@ vg_status run_verify(const Shape& s, const vg_kv_cache* c, const VerifyArgs& a, 
   p.K = static_cast<__nv_bfloat16*>(c->K);
   p.V = static_cast<__nv_bfloat16*>(c->V);
   p.seq_offset = c->seq_offset;
+  p.ptab = c->page_table;
+  p.psize = c->page_table ? c->page_size : 1;
+  p.pstride = c->page_table ? c->pages_per_seq : 0;
+  p.box_rows = verify_box_rows(c);
   p.prefix_len = a.prefix_len;
   p.capacity = c->capacity_slots;
   p.B = s.B;
@@ -372,6 +397,9 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.K = static_cast<__nv_bfloat16*>(c->K);
   p.V = static_cast<__nv_bfloat16*>(c->V);
   p.seq_offset = c->seq_offset;
+  p.ptab = c->page_table;
+  p.psize = c->page_table ? c->page_size : 1;
+  p.pstride = c->page_table ? c->pages_per_seq : 0;
   p.capacity = c->capacity_slots;
   p.idx = a.idx;
   p.count = a.count;
@@ -454,6 +482,7 @@ vg_status iteration_prepare(const vg_dims* dims, const vg_kv_cache* cache, const
   if (st != VG_OK) return st;
   const Shape& s = c->s;
   if ((st = check_cache(cache)) != VG_OK) return st;
+  if ((st = check_verify_pages(cache)) != VG_OK) return st;
   if (!in || !out) return fail(VG_ERR_INVALID_ARG, "inputs and outputs must be non-NULL");
   if (k < 1) return fail(VG_ERR_INVALID_ARG, "k=%d < 1", k);
   if (row_mask0 == 0) return fail(VG_ERR_INVALID_ARG, "row_mask0 (the selection rows) must be non-zero");
@@ -584,6 +613,7 @@ vg_status vg_verify_attn(const vg_dims* dims, const vg_kv_cache* cache, const vo
   vg_status st = check_dims(dims, &s);
   if (st != VG_OK) return st;
   if ((st = check_cache(cache)) != VG_OK) return st;
+  if ((st = check_verify_pages(cache)) != VG_OK) return st;
   VerifyArgs a{q, k_new, v_new, prefix_len, row_mask0, row_mask1, scores0, scores1, score_stride, out};
   if ((st = check_verify_args(s, a)) != VG_OK) return st;
   if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0) return fail(VG_ERR_INVALID_ARG, "dev_status must be 4-byte aligned");

@@ -281,6 +281,38 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Physical slot of logical token i of sequence b in the KV cache, or -1 when it falls
+// outside the cache.  Without a page table the slot pool holds sequence b from slot
+// seq_offset[b] on; with one, token i lives at row i mod page_size of physical page
+// page_table[b][i / page_size] (pages of page_size slots: page p spans slots
+// p * page_size .. p * page_size + page_size - 1).  L2_ONLY loads bypass L1 (the draft
+// step resolves slots before its dependency wait when its selection is settled, and must
+// see what kernels that completed earlier wrote).
+template <bool L2_ONLY = false>
+__device__ __forceinline__ int64_t kv_slot(const int64_t* seq_offset, const int32_t* ptab, int psize, int pstride,
+                                           int64_t capacity, int b, int64_t i) {
+  if (i < 0) return -1;
+  if (ptab == nullptr) {
+    const int64_t s = (L2_ONLY ? __ldcg(seq_offset + b) : seq_offset[b]) + i;
+    return s >= 0 && s < capacity ? s : -1;
+  }
+  if (i >= static_cast<int64_t>(pstride) * psize) return -1;
+  // (32-bit arithmetic: i < 2^31; a shift for the usual power-of-two page sizes)
+  const int ii = static_cast<int>(i);
+  int pi, row;
+  if ((psize & (psize - 1)) == 0) {
+    const int sh = __ffs(psize) - 1;
+    pi = ii >> sh;
+    row = ii & (psize - 1);
+  } else {
+    pi = ii / psize;
+    row = ii - pi * psize;
+  }
+  const int32_t* e = ptab + static_cast<int64_t>(b) * pstride + pi;
+  const int64_t pg = L2_ONLY ? __ldcg(e) : *e;
+  return pg >= 0 && (pg + 1) * psize <= capacity ? pg * psize + row : -1;
+}
+
 // CTA of a balanced contiguous split of T items over N CTAs that owns item x:
 // CTA c owns [floor(c T / N), floor((c+1) T / N)).  (A 64-bit division is a long
 // instruction sequence on the GPU: when the products fit in 32 bits, as they do for

@@ -27,7 +27,10 @@ struct VerifyParams {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* K;            // cache [capacity][Hkv][D]
   __nv_bfloat16* V;
-  const int64_t* seq_offset;   // [B]
+  const int64_t* seq_offset;   // [B] (slot pool) or null (paged)
+  const int32_t* ptab;         // [B][pstride] page table, or null (slot pool)
+  int psize, pstride;          // tokens per page, pages per sequence
+  int box_rows;                // rows of one K/V TMA box: 64 for the slot pool, else min(page size, 64)
   const int32_t* prefix_len;   // [B]
   int64_t capacity;
   int B, Hq, Hkv, G, R, D, M, Mpad;  // M = G * R rows per KV head, Mpad = 16 * ceil(M / 16)
@@ -68,7 +71,9 @@ struct DraftParams {
   const __nv_bfloat16* v_new;
   __nv_bfloat16* K;
   __nv_bfloat16* V;
-  const int64_t* seq_offset;
+  const int64_t* seq_offset;   // [B] (slot pool) or null (paged)
+  const int32_t* ptab;         // [B][pstride] page table, or null (slot pool)
+  int psize, pstride;
   int64_t capacity;
   const int32_t* idx;          // [B][k_stride]
   const int32_t* count;        // [B]

@@ -50,7 +50,13 @@ class LayerState:
         self.k_draft = bf16_tensor(pool["k_draft"], dev)
         self.v_draft = bf16_tensor(pool["v_draft"], dev)
         self.dims = vb.make_dims(self.B, self.Hq, self.Hkv, self.d, self.gamma, self.max_len)
-        self.cache = vb.make_cache(self.K, self.V, self.seq_offset)
+        if "page_table" in pool:  # a paged layout of the same layer (seq_offset then unused)
+            self.page_table = torch.from_numpy(pool["page_table"].astype(np.int32)).to(dev)
+            self.cache = vb.make_cache(self.K, self.V, None, page_table=self.page_table,
+                                       page_size=int(pool["page_size"]))
+        else:
+            self.page_table = None
+            self.cache = vb.make_cache(self.K, self.V, self.seq_offset)
         R = self.gamma + 1
         self.score_stride = max(4, (self.max_len + 3) // 4 * 4)
         self.out_verify = torch.empty(self.B, R, self.Hq, self.d, dtype=torch.bfloat16, device=dev)

@@ -299,6 +299,38 @@ WORKLOADS = {
 }
 
 
+# ---------------------------------------------------------------- paged layout
+def to_paged(w: "Workload", pool: dict, page_size: int, seed: int = 0) -> dict:
+    """The same layer laid out as a paged cache: every sequence's tokens (prefix plus the
+    gamma+1 verify rows) in pages of page_size slots, the pages of all sequences spread
+    over the pool by a seeded permutation (seed None: in order, an identity table).  Returns the pool dict with K and V
+    re-arranged, page_table int32 [B][pages_per_seq] and page_size; the logical content
+    is unchanged (layout only, no attention arithmetic)."""
+    n = pool["prefix_len"].astype(np.int64)
+    need = (n + w.R + page_size - 1) // page_size                  # pages per sequence
+    pages_per_seq = int(need.max())
+    total = int(need.sum())
+    perm = np.arange(total) if seed is None else np.random.default_rng(seed).permutation(total)
+    table = np.full((w.B, pages_per_seq), -1, dtype=np.int32)
+    K = np.zeros((total * page_size,) + pool["K"].shape[1:], dtype=np.uint16)
+    V = np.zeros_like(K)
+    k = 0
+    for b in range(w.B):
+        o = int(pool["seq_offset"][b])
+        cap = int(pool["seq_offset"][b + 1]) - o if b + 1 < w.B else pool["K"].shape[0] - o
+        for j in range(int(need[b])):
+            pg = int(perm[k])
+            k += 1
+            table[b, j] = pg
+            lo, hi = j * page_size, min((j + 1) * page_size, cap)
+            if lo < hi:
+                K[pg * page_size:pg * page_size + hi - lo] = pool["K"][o + lo:o + hi]
+                V[pg * page_size:pg * page_size + hi - lo] = pool["V"][o + lo:o + hi]
+    out = dict(pool)
+    out.update(K=K, V=V, page_table=table, page_size=page_size, slots=total * page_size)
+    return out
+
+
 # ---------------------------------------------------------------- acceptance inputs
 def accept_inputs(B: int, gamma: int, V: int, seed: int, scale: float = 3.0, noise: float = 1.0) -> dict:
     """Synthetic inputs of the acceptance step (fp32 logits, as a model's output head

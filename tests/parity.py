@@ -54,6 +54,15 @@ def assert_topk_exact(gpu_idx: np.ndarray, gpu_count: int, gpu_scores_f32: np.nd
     return want
 
 
+def token_slots(pool: dict, b: int, count: int) -> np.ndarray:
+    """Physical cache slots of tokens 0..count-1 of sequence b: the slot pool from
+    seq_offset[b] on, or the pages of a paged layout."""
+    if "page_table" in pool:
+        return oracle.paged_slots(pool["page_table"][b], int(pool["page_size"]), count)
+    o = int(pool["seq_offset"][b])
+    return np.arange(o, o + count)
+
+
 def check_iteration(w, pool: dict, st, rows0, rows1, check_draft: bool = True,
                     seqs=None) -> dict:
     """Compare one vg_iteration on the GPU with the oracle, sequence by sequence."""
@@ -71,9 +80,10 @@ def check_iteration(w, pool: dict, st, rows0, rows1, check_draft: bool = True,
     Vc = bf16_to_f64(st.V)
     stats = {"overlap": []}
     for b in (range(w.B) if seqs is None else seqs):
-        o, n = int(pool["seq_offset"][b]), int(pool["prefix_len"][b])
-        K = widen_bf16(pool["K"][o:o + n])
-        V = widen_bf16(pool["V"][o:o + n])
+        n = int(pool["prefix_len"][b])
+        sl = token_slots(pool, b, n + w.R)
+        K = widen_bf16(pool["K"][sl[:n]])
+        V = widen_bf16(pool["V"][sl[:n]])
         q = widen_bf16(pool["q_verify"][b])
         kn, vn = widen_bf16(pool["k_new"][b]), widen_bf16(pool["v_new"][b])
         ref = oracle.verify_attention(q, K, V, kn, vn)
@@ -95,9 +105,9 @@ def check_iteration(w, pool: dict, st, rows0, rows1, check_draft: bool = True,
                 ref_d = oracle.draft_step(qd[s], K, V, T, kd[:s + 1], vd[:s + 1])
                 assert_attn_close(out_d[s, b], ref_d, f"draft step {s} seq {b}")
             # the cache now holds draft tokens at n..n+gamma-1 and verify row gamma at n+gamma
-            assert np.array_equal(Kc[o + n:o + n + w.gamma], kd), f"draft K append seq {b}"
-            assert np.array_equal(Vc[o + n:o + n + w.gamma], vd), f"draft V append seq {b}"
-        assert np.array_equal(Kc[o + n + w.gamma], kn[w.gamma]), f"verify K append seq {b}"
-        assert np.array_equal(Vc[o + n + w.gamma], vn[w.gamma]), f"verify V append seq {b}"
-        assert np.array_equal(Kc[o:o + n], K), f"prefix K modified seq {b}"
+            assert np.array_equal(Kc[sl[n:n + w.gamma]], kd), f"draft K append seq {b}"
+            assert np.array_equal(Vc[sl[n:n + w.gamma]], vd), f"draft V append seq {b}"
+        assert np.array_equal(Kc[sl[n + w.gamma]], kn[w.gamma]), f"verify K append seq {b}"
+        assert np.array_equal(Vc[sl[n + w.gamma]], vn[w.gamma]), f"verify V append seq {b}"
+        assert np.array_equal(Kc[sl[:n]], K), f"prefix K modified seq {b}"
     return stats

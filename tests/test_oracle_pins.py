@@ -343,6 +343,27 @@ def test_window_is_the_topk_of_a_recency_score():
         assert oracle.select_topk(s, k).tolist() == oracle.select_window(n, k).tolist()
 
 
+# ------------------------------------------------------------ paged cache
+def test_paged_slots_hand_case():
+    # pages of 2 tokens, sequence in pages 3 then 0
+    assert oracle.paged_slots(np.array([3, 0]), 2, 4).tolist() == [6, 7, 0, 1]
+    assert oracle.paged_slots(np.array([3, 0]), 2, 3).tolist() == [6, 7, 0]
+
+
+def test_page_size_one_takes_the_table_as_token_slots():
+    # Vegas §3: with pages of one token, the page indices are the token slots themselves
+    t = np.array([9, 2, 5, 7])
+    assert oracle.paged_slots(t, 1, 4).tolist() == t.tolist()
+
+
+def test_identity_table_is_the_flat_pool():
+    for P in (1, 8, 16, 64):
+        o = 5 * P
+        n = 3 * P + 7
+        table = np.arange(o // P, o // P + (n + P - 1) // P)
+        assert oracle.paged_slots(table, P, n).tolist() == list(range(o, o + n))
+
+
 # ------------------------------------------------------------ planted mistakes
 def _pin_errors(mod):
     """Discrepancies of the pins above for a (possibly mutated) oracle module."""
@@ -369,6 +390,7 @@ def _pin_errors(mod):
     sparse = mod.draft_step(q[2], K, V, np.arange(n), kn[:3], vn[:3])
     errs["k_eq_n"] = np.abs(dense - sparse).max()
     errs["overlap"] = abs(mod.selection_overlap(np.array([0, 2, 4, 6]), np.array([2, 3, 4, 5]), 4) - 0.5)
+    errs["paged"] = int(mod.paged_slots(np.array([3, 0]), 2, 4).tolist() != [6, 7, 0, 1])
     errs["window"] = int(mod.select_window(10, 3).tolist() != [7, 8, 9]) + int(
         mod.select_topk(np.arange(1.0, 13.0), 5).tolist() != mod.select_window(12, 5).tolist())
     return errs
@@ -376,7 +398,8 @@ def _pin_errors(mod):
 
 def _caught(errs):
     return (errs["sdpa"] > 1e-9 or errs["linearity"] > 1e-9 or errs["worked"] > 1e-9
-            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9 or errs["overlap"] > 0 or errs["window"] > 0)
+            or errs["brute"] > 0 or errs["k_eq_n"] > 1e-9 or errs["overlap"] > 0 or errs["window"] > 0
+            or errs["paged"] > 0)
 
 
 def test_unmutated_oracle_passes_every_pin():
@@ -395,6 +418,7 @@ MUTANTS = {
     "overlap over the larger total": ("selection_overlap", None, None),
     "window one position early": ("select_window", None, None),
     "window at the start": ("select_window", None, None),
+    "page rows transposed": ("paged_slots", None, None),
 }
 
 
@@ -463,6 +487,11 @@ def _mutant(name):
         def select_window(n, k):
             return np.arange(0, min(k, n), dtype=np.int64)
         m.select_window = select_window
+    elif name == "page rows transposed":
+        def paged_slots(table_row, page_size, n):
+            i = np.arange(n, dtype=np.int64)
+            return np.asarray(table_row, dtype=np.int64)[i % len(table_row)] * page_size + i // len(table_row)
+        m.paged_slots = paged_slots
     return m
 
 
