@@ -73,9 +73,49 @@ __device__ __forceinline__ void qk16(const uint32_t (&qf)[D / 16][4], KAddr kadd
 // each multiplied with the same value fragments, so the weights carry about 16 bits
 // (relative error near 2^-17) and agree with the fp32 row sum l: rounding P to bf16
 // alone would move a row whose weight sits on a few keys by up to 2^-9 of its values.
-template <int D, typename VAddr>
+//
+// PACK (at most 8 query rows, so rows 8..15 hold no query): the low part of row r
+// takes the A-operand row r + 8, and one MMA per value block yields both products,
+// the high part's in accumulator rows 0..7 and the low part's in rows 8..15; the
+// output of row r is then o[.][0..1] + o[.][2..3] (fold_packed).
+template <int D, bool PACK = false, typename VAddr>
 __device__ __forceinline__ void softmax_pv16(RowState<D>& st, float (&s)[2][4], VAddr vaddr, int lane) {
   const float NEG = neg_inf();
+  if constexpr (PACK) {
+    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    const float mn0 = fmaxf(st.m[0], mx0);
+    const float mu0 = mn0 == NEG ? 0.f : mn0;
+    if (__any_sync(0xffffffffu, mn0 > st.m[0])) {
+      const float a0 = ex2(st.m[0] - mu0);
+      st.l[0] *= a0;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        st.o[dn][0] *= a0;
+        st.o[dn][1] *= a0;
+        st.o[dn][2] *= a0;
+        st.o[dn][3] *= a0;
+      }
+    }
+    st.m[0] = mn0;
+    const float p00 = ex2(s[0][0] - mu0), p01 = ex2(s[0][1] - mu0);
+    const float p10 = ex2(s[1][0] - mu0), p11 = ex2(s[1][1] - mu0);
+    st.l[0] += p00 + p01 + p10 + p11;
+    uint32_t a[4];  // rows r: high part, rows r + 8: low part (keys 0..7, then 8..15)
+    split_bf16(p00, p01, a[0], a[1]);
+    split_bf16(p10, p11, a[2], a[3]);
+    const int mi = lane >> 3, rr = lane & 7;
+    const int r = (mi & 1) * 8 + rr;
+#pragma unroll
+    for (int dn2 = 0; dn2 < D / 16; ++dn2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vaddr(r, dn2 * 2 + (mi >> 1)), b0, b1, b2, b3);
+      mma_bf16(st.o[2 * dn2], a, b0, b1);
+      mma_bf16(st.o[2 * dn2 + 1], a, b2, b3);
+    }
+    return;
+  }
   float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
   float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
   mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -123,6 +163,17 @@ __device__ __forceinline__ void softmax_pv16(RowState<D>& st, float (&s)[2][4], 
     mma_bf16(st.o[2 * dn2 + 1], ph, b2, b3);
     mma_bf16(st.o[2 * dn2], pl, b0, b1);
     mma_bf16(st.o[2 * dn2 + 1], pl, b2, b3);
+  }
+}
+
+// Output rows of a PACK state: adds the low part's products (rows 8..15) to the high
+// part's (rows 0..7).
+template <int D>
+__device__ __forceinline__ void fold_packed(RowState<D>& st) {
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn) {
+    st.o[dn][0] += st.o[dn][2];
+    st.o[dn][1] += st.o[dn][3];
   }
 }
 

@@ -42,15 +42,29 @@ constexpr int kKeys = 16;  // entries per pipeline stage (one MMA key block)
 constexpr int kStages = 2;
 constexpr int kCombineRows = 12;  // partial rows a combine warp loads in one round
 
+constexpr int kBatch = 128;  // entries the producer resolves in one round of loads (4 a lane)
+constexpr int kTab = 256;    // ring of resolved entries (two batches)
+
+// One resolved entry: its position (-1: masked), whether it is a draft-token slot
+// (appended by earlier steps, or the current token, read from the inputs), and where
+// its K and V pages are.
+struct Entry {
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int pos;
+  int tail;
+};
+
 struct DLayout {
   int row;  // bytes per gathered page in shared memory (padded by 16: ldmatrix rows hit distinct banks)
-  int half, stage, off_pos, off_bar, total;
+  int half, stage, off_pos, off_tab, off_bar, total;
   __host__ __device__ DLayout(int Hkv, int D) {
     row = Hkv * D * 2 + 16;
     half = kKeys * row;
     stage = 2 * half;
-    off_pos = kStages * stage;                           // int [kStages][kKeys]
-    off_bar = (off_pos + kStages * kKeys * 4 + 7) & ~7;  // full[kStages], empty[kStages]
+    off_pos = kStages * stage;                             // int [kStages][kKeys]
+    off_tab = (off_pos + kStages * kKeys * 4 + 15) & ~15;  // Entry [kTab]
+    off_bar = off_tab + kTab * static_cast<int>(sizeof(Entry));  // full[kStages], empty[kStages]
     total = off_bar + 2 * kStages * 8;
   }
 };
@@ -86,62 +100,98 @@ __host__ __device__ __forceinline__ SeqSpan seq_span(int b, int S, int64_t E, in
                  static_cast<int>(owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, nctas))};
 }
 
-// One chunk entry as the producer warp resolves it (lane < nvalid: entry slot j + lane
-// of sequence b).  pos = -1 for a masked slot; tail marks a draft-token slot (appended
-// by earlier steps, or the current token, read from the inputs).
-struct ChunkPos {
-  int pos;
-  bool tail;
-  const __nv_bfloat16* ksrc;
-  const __nv_bfloat16* vsrc;
+// The loads behind a batch of entries (entry e = xb + lane + 32 i of the CTA's items),
+// all independent, so one round trip serves the batch.  (They bypass L1, cached at L2
+// only: with a settled selection they run before the dependency wait, and must see
+// what kernels that completed earlier wrote.)
+struct RawBatch {
+  int sel[kBatch / 32], cnt[kBatch / 32], tl[kBatch / 32], ts[kBatch / 32];
+  int64_t so[kBatch / 32];  // seq_offset of the entry's sequence (flat caches)
 };
 
-// (The loads bypass L1, cached at L2 only: with a settled selection they run before the
-// dependency wait, and must see what kernels that completed earlier wrote.)
-template <int D>
-__device__ __forceinline__ ChunkPos resolve(const DraftParams& p, int b, int j, int nvalid, int S, int lane) {
-  const int jj = j + lane;  // selected entries first, then the draft-token tail
-  const int cnt_raw = __ldcg(p.count + b);
-  const int tl = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
-  const int ts = __ldcg(p.tail_start + b);
-  const int sel = (lane < nvalid && jj < p.k_stride) ? __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj) : 0;
-  const bool seq_ok = cnt_raw >= 0 && cnt_raw <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && cnt_raw + tl <= S &&
-                      ts >= 0 && (p.k_new == nullptr || tl >= 1);
-  if (!seq_ok && lane == 0 && j == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
-  const int nsel = seq_ok ? cnt_raw : 0;
-  ChunkPos c{-1, false, nullptr, nullptr};
-  if (seq_ok && lane < nvalid) {
-    if (jj < nsel) {
-      c.pos = sel;
-      if (c.pos < 0 || c.pos >= ts) {
-        report(p.status, VG_ERR_DEVICE_BOUNDS);
-        c.pos = -1;
-      }
-    } else if (jj < nsel + tl) {
-      c.pos = ts + (jj - nsel);
-      c.tail = true;
+__device__ __forceinline__ void load_batch(const DraftParams& p, RawBatch& r, int xb, int x1, int S, int lane) {
+#pragma unroll
+  for (int i = 0; i < kBatch / 32; ++i) {
+    const int e = xb + lane + 32 * i;
+    r.sel[i] = r.cnt[i] = r.tl[i] = r.ts[i] = 0;
+    r.so[i] = 0;
+    if (e < x1) {
+      const int b = e / S, jj = e - b * S;
+      r.cnt[i] = __ldcg(p.count + b);
+      r.tl[i] = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
+      r.ts[i] = __ldcg(p.tail_start + b);
+      if (jj < p.k_stride) r.sel[i] = __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj);
+      if (p.ptab == nullptr) r.so[i] = __ldcg(p.seq_offset + b);
     }
   }
-  if (c.pos >= 0) {
-    if (p.k_new && c.pos == ts + tl - 1) {  // the current draft token, straight from the inputs
-      c.ksrc = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
-      c.vsrc = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
-    } else {
-      const int64_t slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, c.pos);
-      if (slot < 0) {  // outside the cache (or the page table): skipped, reported
-        report(p.status, VG_ERR_DEVICE_BOUNDS);
-        c.pos = -1;
-      } else {
-        c.ksrc = p.K + static_cast<size_t>(slot) * p.Hkv * D;
-        c.vsrc = p.V + static_cast<size_t>(slot) * p.Hkv * D;
-      }
-    }
-  }
-  return c;
 }
 
-// MAXW: the most KV heads (consumer warps) this instantiation serves.
-template <int D, int MAXW>
+// Turns a loaded batch into table entries (ring slot (e - x0) mod kTab).  Entry slot jj
+// of sequence b: its selected entries first, then the draft-token tail; a paged cache
+// looks each position's page up (a second round trip, the page number depending on it).
+template <int D>
+__device__ __forceinline__ void finish_batch(const DraftParams& p, const RawBatch& r, Entry* tab, int x0, int xb,
+                                             int x1, int S, int lane) {
+  int pos[kBatch / 32], tail[kBatch / 32];
+#pragma unroll
+  for (int i = 0; i < kBatch / 32; ++i) {
+    const int e = xb + lane + 32 * i;
+    pos[i] = -1;
+    tail[i] = 0;
+    if (e < x1) {
+      const int b = e / S, jj = e - b * S;
+      const int cnt = r.cnt[i], tl = r.tl[i], ts = r.ts[i];
+      const bool seq_ok = cnt >= 0 && cnt <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && cnt + tl <= S &&
+                          ts >= 0 && (p.k_new == nullptr || tl >= 1);
+      if (!seq_ok && jj == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
+      if (seq_ok) {
+        if (jj < cnt) {
+          pos[i] = r.sel[i];
+          if (pos[i] < 0 || pos[i] >= ts) {
+            report(p.status, VG_ERR_DEVICE_BOUNDS);
+            pos[i] = -1;
+          }
+        } else if (jj < cnt + tl) {
+          pos[i] = ts + (jj - cnt);
+          tail[i] = 1;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kBatch / 32; ++i) {
+    const int e = xb + lane + 32 * i;
+    if (e >= x1) continue;
+    Entry t{nullptr, nullptr, pos[i], tail[i]};
+    if (t.pos >= 0) {
+      const int b = e / S;
+      if (p.k_new && t.tail && t.pos == r.ts[i] + r.tl[i] - 1) {  // the current draft token, from the inputs
+        t.k = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
+        t.v = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
+      } else {
+        int64_t slot;
+        if (p.ptab == nullptr) {
+          const int64_t s2 = r.so[i] + t.pos;
+          slot = s2 >= 0 && s2 < p.capacity ? s2 : -1;
+        } else {
+          slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, t.pos);
+        }
+        if (slot < 0) {  // outside the cache (or the page table): skipped, reported
+          report(p.status, VG_ERR_DEVICE_BOUNDS);
+          t.pos = -1;
+        } else {
+          t.k = p.K + static_cast<size_t>(slot) * p.Hkv * D;
+          t.v = p.V + static_cast<size_t>(slot) * p.Hkv * D;
+        }
+      }
+    }
+    tab[(e - x0) & (kTab - 1)] = t;
+  }
+}
+
+// MAXW: the most KV heads (consumer warps) this instantiation serves; PACK: at most 8
+// query heads a KV head (their P high and low parts share one MMA).
+template <int D, int MAXW, bool PACK>
 __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -179,40 +229,62 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
 
   // ------------------------------------------------------------------ producer warp
   if (warp == W) {
+    Entry* tab = reinterpret_cast<Entry*>(smem + L.off_tab);
+    // Entries are resolved a batch ahead: batch n's table entries are written when the
+    // chunks reach it, while batch n + 1's loads are already in flight.
+    RawBatch raw;
+    int res_end = x0;  // entries [x0, res_end) are in the table
+    auto advance_tables = [&]() {
+      finish_batch<D>(p, raw, tab, x0, res_end, x1, S, lane);
+      res_end = min(x1, res_end + kBatch);
+      if (res_end < x1) load_batch(p, raw, res_end, x1, S, lane);
+      __syncwarp();
+    };
+    // Chunk [x, x + nvalid) into stage st: its positions for the consumers, the byte
+    // count on the stage's barrier and the copies.  part: 0 all pages, 1 all but the
+    // draft-token slots, 2 only those (for a chunk whose part 1 is already issued).
+    auto issue_chunk = [&](int st, int x, int nvalid, int part) {
+      const Entry t = lane < nvalid ? tab[(x + lane - x0) & (kTab - 1)] : Entry{nullptr, nullptr, -1, 0};
+      if (part != 2) {
+        if (lane < kKeys) posb[st * kKeys + lane] = t.pos;
+        const int nload = __popc(__ballot_sync(0xffffffffu, t.pos >= 0));
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nload * 2 * page));
+        __syncwarp();
+      }
+      if (t.pos >= 0 && (part == 0 || (part == 1) == !t.tail)) {
+        uint8_t* kst = smem + st * L.stage;
+        bulk_load(kst + lane * L.row, t.k, page, &full[st]);
+        bulk_load(kst + L.half + lane * L.row, t.v, page, &full[st]);
+      }
+    };
     int b = x0 / S, j = x0 - b * S;
+    int x = x0;
     int stage = 0;
     uint32_t phase = 0;
-    int issued = 0;  // chunks whose copies were started
-    // With a settled selection the first kStages chunks' positions are resolved and
-    // their selected pages requested before the dependency wait; their tail pages (the
-    // previous step appended the last of them) and every later chunk wait for it.
-    ChunkPos early[kStages];
+    int issued;  // chunks whose copies were started
+    // With a settled selection the first chunks (as many as the ring holds) are resolved
+    // and their selected pages requested before the dependency wait; their draft-token
+    // pages (the previous step appended the last of them) and every later chunk wait
+    // for it.
+    int ex[kStages], en[kStages];
     int nearly = 0;
     if (p.settled) {
-      int bb = b, jj0 = j, x = x0;
+      load_batch(p, raw, x0, x1, S, lane);
+      advance_tables();
 #pragma unroll
       for (int i = 0; i < kStages; ++i) {
-        early[i] = ChunkPos{-1, false, nullptr, nullptr};
         if (x < x1) {
-          const int nvalid = min(kKeys, min(x1 - x, S - jj0));
-          const ChunkPos c = resolve<D>(p, bb, jj0, nvalid, S, lane);
-          if (lane < kKeys) posb[i * kKeys + lane] = c.pos;
-          const int nload = __popc(__ballot_sync(0xffffffffu, c.pos >= 0));
-          __syncwarp();
-          if (lane == 0) mbar_arrive_expect_tx(&full[i], static_cast<uint32_t>(nload * 2 * page));
-          __syncwarp();
-          if (c.pos >= 0 && !c.tail) {
-            uint8_t* kst = smem + i * L.stage;
-            bulk_load(kst + lane * L.row, c.ksrc, page, &full[i]);
-            bulk_load(kst + L.half + lane * L.row, c.vsrc, page, &full[i]);
-          }
-          early[i] = c;
+          const int nvalid = min(kKeys, min(x1 - x, S - j));
+          issue_chunk(i, x, nvalid, 1);
+          ex[i] = x;
+          en[i] = nvalid;
           nearly = i + 1;
           x += nvalid;
-          jj0 += nvalid;
-          if (jj0 == S) {
-            jj0 = 0;
-            ++bb;
+          j += nvalid;
+          if (j == S) {
+            j = 0;
+            ++b;
           }
         }
       }
@@ -225,32 +297,23 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     // order a chain of early triggers could run a later step ahead of it).
     pdl_wait();
     pdl_launch_dependents();
-#pragma unroll
-    for (int i = 0; i < kStages; ++i) {
-      if (i < nearly && early[i].pos >= 0 && early[i].tail) {
-        uint8_t* kst = smem + i * L.stage;
-        bulk_load(kst + lane * L.row, early[i].ksrc, page, &full[i]);
-        bulk_load(kst + L.half + lane * L.row, early[i].vsrc, page, &full[i]);
-      }
+    if (!p.settled) {
+      load_batch(p, raw, x0, x1, S, lane);
+      advance_tables();
     }
-    for (int x = x0; x < x1;) {
+#pragma unroll
+    for (int i = 0; i < kStages; ++i)
+      if (i < nearly) issue_chunk(i, ex[i], en[i], 2);
+    issued = nearly;
+    stage = nearly % kStages;
+    phase = static_cast<uint32_t>((nearly / kStages) & 1);
+    while (x < x1) {
       const int nvalid = min(kKeys, min(x1 - x, S - j));
-      if (issued >= nearly) {
-        bool ok_wait = true;
-        if (lane == 0 && issued >= kStages) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
-        if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
-        const ChunkPos c = resolve<D>(p, b, j, nvalid, S, lane);
-        if (lane < kKeys) posb[stage * kKeys + lane] = c.pos;
-        const int nload = __popc(__ballot_sync(0xffffffffu, c.pos >= 0));
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nload * 2 * page));
-        __syncwarp();
-        if (c.pos >= 0) {
-          uint8_t* kst = smem + stage * L.stage;
-          bulk_load(kst + lane * L.row, c.ksrc, page, &full[stage]);
-          bulk_load(kst + L.half + lane * L.row, c.vsrc, page, &full[stage]);
-        }
-      }
+      if (x + nvalid > res_end) advance_tables();
+      bool ok_wait = true;
+      if (lane == 0 && issued >= kStages) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
+      if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
+      issue_chunk(stage, x, nvalid, 0);
       ++issued;
       x += nvalid;
       j += nvalid;
@@ -312,7 +375,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
           s[nt][c] = ok ? s[nt][c] * p.scale_log2 : NEG;
           s[nt][2 + c] = ok ? s[nt][2 + c] * p.scale_log2 : NEG;
         }
-      softmax_pv16<D>(st, s, vaddr, lane);
+      softmax_pv16<D, PACK>(st, s, vaddr, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
       if (++stage == kStages) {
@@ -323,6 +386,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
       j += nvalid;
     }
     if (lost) x = seg_end;  // (results of a lost wait are unspecified; the status says so)
+    if constexpr (PACK) fold_packed<D>(st);
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], 1);
     st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], 2);
     st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], 1);
@@ -480,10 +544,10 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   }
 }
 
-template <int D, int MAXW>
+template <int D, int MAXW, bool PACK>
 cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) {
   const size_t smem = static_cast<size_t>(DLayout(p.Hkv, D).total) + 128;
-  cudaError_t e = ensure_smem<draft_kernel<D, MAXW>>(smem);
+  cudaError_t e = ensure_smem<draft_kernel<D, MAXW, PACK>>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -495,7 +559,7 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  if ((e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW>, p)) != cudaSuccess) return e;
+  if ((e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW, PACK>, p)) != cudaSuccess) return e;
   const int nw = draft_combine_warps(p.B, p.slots, p.nctas);
   if (nw == 0) return cudaSuccess;  // every sequence was finished by the CTA holding it
   cudaLaunchConfig_t cfg2 = {};
@@ -527,11 +591,13 @@ int draft_combine_warps(int B, int slots, int nctas) {
 }
 
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl) {
+  const bool pack = p.G <= 8;
   if (p.Hkv <= 8) {
-    if (p.D == 64) return launch_draft_t<64, 8>(p, stream, pdl);
-    if (p.D == 128) return launch_draft_t<128, 8>(p, stream, pdl);
+    if (p.D == 64) return pack ? launch_draft_t<64, 8, true>(p, stream, pdl) : launch_draft_t<64, 8, false>(p, stream, pdl);
+    if (p.D == 128)
+      return pack ? launch_draft_t<128, 8, true>(p, stream, pdl) : launch_draft_t<128, 8, false>(p, stream, pdl);
   } else if (p.D == 64) {  // (more than 8 KV heads at d = 128 exceed a 1024-element page)
-    return launch_draft_t<64, 16>(p, stream, pdl);
+    return pack ? launch_draft_t<64, 16, true>(p, stream, pdl) : launch_draft_t<64, 16, false>(p, stream, pdl);
   }
   return cudaErrorInvalidValue;
 }
