@@ -13,18 +13,22 @@
 //     the sequence's entries masked - split evenly over one persistent CTA per SM, so
 //     the split needs no device data and each CTA's first round trip fetches its
 //     positions.
+//   * Every thread resolves one of the CTA's first entries (position, cache slot) into
+//     a shared-memory table during the set-up; the producer warp resolves later
+//     entries a batch ahead, so no position round trip sits on the per-chunk path.
 //   * A producer warp turns each entry into two bulk copies of a whole page (large
 //     requests keep the copy engine efficient; the current draft token comes straight
 //     from the inputs) into a padded shared-memory ring guarded by mbarriers; one
 //     consumer warp per KV head runs Q K^T and P V on bf16 tensor cores with fp32
 //     online softmax, P carried as a bf16 high and low part.
 //   * Within a draft phase the selection does not change between steps.  When the
-//     caller says so (VG_DRAFT_SELECTION_SETTLED), the producer resolves its first
-//     chunks' positions and starts their page copies before the dependency wait, so
-//     the gather overlaps the end of the previous step; only the draft-token tail,
-//     which the previous step appended, waits for it.  Both kernels here release
-//     their dependents only after their own dependency wait, so no draft step starts
-//     before every kernel two launches back has completed.
+//     caller says so (VG_DRAFT_SELECTION_SETTLED), the CTA resolves its first entries
+//     and the producer starts their page copies before the dependency wait, so the
+//     gather overlaps the end of the previous step; only the draft-token tail, which
+//     the previous step appended, waits for it.  The draft kernel releases its
+//     dependents only after its own dependency wait, the combine at entry (its set-up
+//     then overlaps the merge): when a draft step starts, the selection kernel and
+//     every step before the previous one have completed.
 //   * A sequence whose entries one CTA holds entirely is finished by that CTA.  Every
 //     other (CTA, sequence) run leaves an unnormalised partial (O, max, sum), and a
 //     combine kernel (programmatic dependent launch) merges each (sequence, query
@@ -100,92 +104,98 @@ __host__ __device__ __forceinline__ SeqSpan seq_span(int b, int S, int64_t E, in
                  static_cast<int>(owner_cta(static_cast<int64_t>(b + 1) * S - 1, E, nctas))};
 }
 
-// The loads behind a batch of entries (entry e = xb + lane + 32 i of the CTA's items),
-// all independent, so one round trip serves the batch.  (They bypass L1, cached at L2
-// only: with a settled selection they run before the dependency wait, and must see
-// what kernels that completed earlier wrote.)
-struct RawBatch {
-  int sel[kBatch / 32], cnt[kBatch / 32], tl[kBatch / 32], ts[kBatch / 32];
-  int64_t so[kBatch / 32];  // seq_offset of the entry's sequence (flat caches)
+// The loads behind entry e of the CTA's items, all independent, so one round trip
+// serves every entry a warp resolves at once.  (They bypass L1, cached at L2 only: with
+// a settled selection they run before the dependency wait, and must see what kernels
+// that completed earlier wrote.)
+struct RawEntry {
+  int sel, cnt, tl, ts;
+  int64_t so;  // seq_offset of the entry's sequence (flat caches)
 };
 
-__device__ __forceinline__ void load_batch(const DraftParams& p, RawBatch& r, int xb, int x1, int S, int lane) {
-#pragma unroll
-  for (int i = 0; i < kBatch / 32; ++i) {
-    const int e = xb + lane + 32 * i;
-    r.sel[i] = r.cnt[i] = r.tl[i] = r.ts[i] = 0;
-    r.so[i] = 0;
-    if (e < x1) {
-      const int b = e / S, jj = e - b * S;
-      r.cnt[i] = __ldcg(p.count + b);
-      r.tl[i] = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
-      r.ts[i] = __ldcg(p.tail_start + b);
-      if (jj < p.k_stride) r.sel[i] = __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj);
-      if (p.ptab == nullptr) r.so[i] = __ldcg(p.seq_offset + b);
-    }
+__device__ __forceinline__ RawEntry load_entry(const DraftParams& p, int e, int x1, int S) {
+  RawEntry r{0, 0, 0, 0, 0};
+  if (e < x1) {
+    const int b = e / S, jj = e - b * S;
+    r.cnt = __ldcg(p.count + b);
+    r.tl = p.tail_len ? __ldcg(p.tail_len + b) : p.tail_len_const;
+    r.ts = __ldcg(p.tail_start + b);
+    if (jj < p.k_stride) r.sel = __ldcg(p.idx + static_cast<size_t>(b) * p.k_stride + jj);
+    if (p.ptab == nullptr) r.so = __ldcg(p.seq_offset + b);
   }
+  return r;
 }
 
-// Turns a loaded batch into table entries (ring slot (e - x0) mod kTab).  Entry slot jj
-// of sequence b: its selected entries first, then the draft-token tail; a paged cache
-// looks each position's page up (a second round trip, the page number depending on it).
+// Entry slot jj of sequence b: its selected entries first, then the draft-token tail.
+// A paged cache looks the position's page up (a second round trip: the page number
+// depends on the position).
 template <int D>
-__device__ __forceinline__ void finish_batch(const DraftParams& p, const RawBatch& r, Entry* tab, int x0, int xb,
-                                             int x1, int S, int lane) {
-  int pos[kBatch / 32], tail[kBatch / 32];
+__device__ __forceinline__ Entry finish_entry(const DraftParams& p, const RawEntry& r, int e, int S) {
+  Entry t{nullptr, nullptr, -1, 0};
+  const int b = e / S, jj = e - b * S;
+  const bool seq_ok = r.cnt >= 0 && r.cnt <= p.k_stride && r.tl >= 0 && r.tl <= kDraftMaxTail && r.cnt + r.tl <= S &&
+                      r.ts >= 0 && (p.k_new == nullptr || r.tl >= 1);
+  if (!seq_ok) {
+    if (jj == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
+    return t;
+  }
+  if (jj < r.cnt) {
+    t.pos = r.sel;
+    if (t.pos < 0 || t.pos >= r.ts) {
+      report(p.status, VG_ERR_DEVICE_BOUNDS);
+      t.pos = -1;
+      return t;
+    }
+  } else if (jj < r.cnt + r.tl) {
+    t.pos = r.ts + (jj - r.cnt);
+    t.tail = 1;
+  } else {
+    return t;
+  }
+  if (p.k_new && t.tail && t.pos == r.ts + r.tl - 1) {  // the current draft token, from the inputs
+    t.k = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
+    t.v = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
+    return t;
+  }
+  int64_t slot;
+  if (p.ptab == nullptr) {
+    const int64_t s2 = r.so + t.pos;
+    slot = s2 >= 0 && s2 < p.capacity ? s2 : -1;
+  } else {
+    slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, t.pos);
+  }
+  if (slot < 0) {  // outside the cache (or the page table): skipped, reported
+    report(p.status, VG_ERR_DEVICE_BOUNDS);
+    t.pos = -1;
+  } else {
+    t.k = p.K + static_cast<size_t>(slot) * p.Hkv * D;
+    t.v = p.V + static_cast<size_t>(slot) * p.Hkv * D;
+  }
+  return t;
+}
+
+// A batch of kBatch entries for the producer warp: entry xb + lane + 32 i.
+__device__ __forceinline__ void load_batch(const DraftParams& p, RawEntry (&r)[kBatch / 32], int xb, int x1, int S,
+                                           int lane) {
+#pragma unroll
+  for (int i = 0; i < kBatch / 32; ++i) r[i] = load_entry(p, xb + lane + 32 * i, x1, S);
+}
+
+// Its table entries, ring slot (e - x0) mod kTab (all resolved before any is stored, so
+// a paged cache's page lookups overlap).
+template <int D>
+__device__ __forceinline__ void finish_batch(const DraftParams& p, const RawEntry (&r)[kBatch / 32], Entry* tab,
+                                             int x0, int xb, int x1, int S, int lane) {
+  Entry t[kBatch / 32];
 #pragma unroll
   for (int i = 0; i < kBatch / 32; ++i) {
     const int e = xb + lane + 32 * i;
-    pos[i] = -1;
-    tail[i] = 0;
-    if (e < x1) {
-      const int b = e / S, jj = e - b * S;
-      const int cnt = r.cnt[i], tl = r.tl[i], ts = r.ts[i];
-      const bool seq_ok = cnt >= 0 && cnt <= p.k_stride && tl >= 0 && tl <= kDraftMaxTail && cnt + tl <= S &&
-                          ts >= 0 && (p.k_new == nullptr || tl >= 1);
-      if (!seq_ok && jj == 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
-      if (seq_ok) {
-        if (jj < cnt) {
-          pos[i] = r.sel[i];
-          if (pos[i] < 0 || pos[i] >= ts) {
-            report(p.status, VG_ERR_DEVICE_BOUNDS);
-            pos[i] = -1;
-          }
-        } else if (jj < cnt + tl) {
-          pos[i] = ts + (jj - cnt);
-          tail[i] = 1;
-        }
-      }
-    }
+    t[i] = e < x1 ? finish_entry<D>(p, r[i], e, S) : Entry{nullptr, nullptr, -1, 0};
   }
 #pragma unroll
   for (int i = 0; i < kBatch / 32; ++i) {
     const int e = xb + lane + 32 * i;
-    if (e >= x1) continue;
-    Entry t{nullptr, nullptr, pos[i], tail[i]};
-    if (t.pos >= 0) {
-      const int b = e / S;
-      if (p.k_new && t.tail && t.pos == r.ts[i] + r.tl[i] - 1) {  // the current draft token, from the inputs
-        t.k = p.k_new + static_cast<size_t>(b) * p.Hkv * D;
-        t.v = p.v_new + static_cast<size_t>(b) * p.Hkv * D;
-      } else {
-        int64_t slot;
-        if (p.ptab == nullptr) {
-          const int64_t s2 = r.so[i] + t.pos;
-          slot = s2 >= 0 && s2 < p.capacity ? s2 : -1;
-        } else {
-          slot = kv_slot<true>(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, b, t.pos);
-        }
-        if (slot < 0) {  // outside the cache (or the page table): skipped, reported
-          report(p.status, VG_ERR_DEVICE_BOUNDS);
-          t.pos = -1;
-        } else {
-          t.k = p.K + static_cast<size_t>(slot) * p.Hkv * D;
-          t.v = p.V + static_cast<size_t>(slot) * p.Hkv * D;
-        }
-      }
-    }
-    tab[(e - x0) & (kTab - 1)] = t;
+    if (e < x1) tab[(e - x0) & (kTab - 1)] = t[i];
   }
 }
 
@@ -203,6 +213,20 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float NEG = neg_inf();
 
+  const int S = p.slots;
+  const int64_t E = static_cast<int64_t>(p.B) * S;
+  const int x0 = static_cast<int>(split_begin(blockIdx.x, E, p.nctas));
+  const int x1 = static_cast<int>(split_begin(blockIdx.x + 1, E, p.nctas));
+  Entry* tab = reinterpret_cast<Entry*>(smem + L.off_tab);
+  // The first entries of the CTA (one a thread, up to the table's size) are resolved
+  // during the set-up, by every thread at once: with a settled selection their loads
+  // are issued first and land while the stages are zeroed; otherwise after the
+  // dependency wait.
+  const int n0 = min(static_cast<int>(blockDim.x), kTab);
+  const int e0 = x0 + static_cast<int>(threadIdx.x);
+  const bool mine = static_cast<int>(threadIdx.x) < n0 && e0 < x1;
+  RawEntry r0{0, 0, 0, 0, 0};
+  if (p.settled && mine) r0 = load_entry(p, e0, x1, S);
   if (threadIdx.x == 32) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -218,22 +242,23 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     uint4* vr = reinterpret_cast<uint4*>(smem + st * L.stage + L.half);
     for (int i = threadIdx.x; i < L.half / 16; i += blockDim.x) vr[i] = make_uint4(0u, 0u, 0u, 0u);
   }
+  if (!p.settled) {
+    pdl_wait();
+    if (mine) r0 = load_entry(p, e0, x1, S);
+  }
+  if (mine) tab[threadIdx.x] = finish_entry<D>(p, r0, e0, S);
   fence_proxy_async_smem();  // the zeros precede the bulk copies into the same stages
   __syncthreads();
-  const int S = p.slots;
-  const int64_t E = static_cast<int64_t>(p.B) * S;
-  const int x0 = static_cast<int>(split_begin(blockIdx.x, E, p.nctas));
-  const int x1 = static_cast<int>(split_begin(blockIdx.x + 1, E, p.nctas));
   if (x0 >= x1) return;
   const int page = p.Hkv * D * 2;  // bytes of one token's K (or V), all heads
 
   // ------------------------------------------------------------------ producer warp
   if (warp == W) {
-    Entry* tab = reinterpret_cast<Entry*>(smem + L.off_tab);
-    // Entries are resolved a batch ahead: batch n's table entries are written when the
-    // chunks reach it, while batch n + 1's loads are already in flight.
-    RawBatch raw;
-    int res_end = x0;  // entries [x0, res_end) are in the table
+    // Later entries are resolved a batch ahead: a batch's table entries are written
+    // when the chunks reach it, while the next batch's loads are already in flight.
+    RawEntry raw[kBatch / 32];
+    int res_end = min(x1, x0 + n0);  // entries [x0, res_end) are in the table
+    if (res_end < x1) load_batch(p, raw, res_end, x1, S, lane);
     auto advance_tables = [&]() {
       finish_batch<D>(p, raw, tab, x0, res_end, x1, S, lane);
       res_end = min(x1, res_end + kBatch);
@@ -263,15 +288,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     int stage = 0;
     uint32_t phase = 0;
     int issued;  // chunks whose copies were started
-    // With a settled selection the first chunks (as many as the ring holds) are resolved
-    // and their selected pages requested before the dependency wait; their draft-token
-    // pages (the previous step appended the last of them) and every later chunk wait
-    // for it.
+    // With a settled selection the first chunks' selected pages (as many chunks as the
+    // ring holds) are requested before the dependency wait; their draft-token pages (the
+    // previous step appended the last of them) and every later chunk wait for it.
     int ex[kStages], en[kStages];
     int nearly = 0;
     if (p.settled) {
-      load_batch(p, raw, x0, x1, S, lane);
-      advance_tables();
 #pragma unroll
       for (int i = 0; i < kStages; ++i) {
         if (x < x1) {
@@ -297,10 +319,6 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     // order a chain of early triggers could run a later step ahead of it).
     pdl_wait();
     pdl_launch_dependents();
-    if (!p.settled) {
-      load_batch(p, raw, x0, x1, S, lane);
-      advance_tables();
-    }
 #pragma unroll
     for (int i = 0; i < kStages; ++i)
       if (i < nearly) issue_chunk(i, ex[i], en[i], 2);
@@ -460,11 +478,13 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
       if (slot >= 0) adst = (slot * p.Hkv + g) * D;
     }
   }
-  // The next draft step may start once the draft kernel before this one completed: a
-  // step with a settled selection gathers before its own dependency wait, which is
-  // safe only when every kernel ahead of it in the chain has finished.
-  pdl_wait();
+  // The next draft step may start its prologue now.  A step with a settled selection
+  // reads the selection and gathers selected pages before its dependency wait: no
+  // kernel still running writes either (this step's appends go to draft-token slots),
+  // and the selection kernel has completed, since every draft kernel releases its
+  // dependents only after its own dependency wait.
   pdl_launch_dependents();
+  pdl_wait();
   if (nseg == 1) return;  // the one CTA holding b finished it
   auto prow = [&](int si) { return (static_cast<size_t>(sp.cf + si) + b) * p.Hq + h; };
   // ---- one round of loads: lane q holds (max, sum) of partial warp + NW q; the first
