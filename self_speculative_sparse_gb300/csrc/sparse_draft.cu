@@ -43,7 +43,8 @@ namespace vg {
 namespace {
 
 constexpr int kKeys = 16;  // entries per pipeline stage (one MMA key block)
-constexpr int kStages = 2;
+constexpr int kMinStages = 2;  // ring stages: 2, or 3 for CTAs with many chunks (the host picks)
+constexpr int kMaxStages = 3;
 constexpr int kCombineRows = 12;  // partial rows a combine warp loads in one round
 
 constexpr int kBatch = 128;  // entries the producer resolves in one round of loads (4 a lane)
@@ -62,14 +63,14 @@ struct Entry {
 struct DLayout {
   int row;  // bytes per gathered page in shared memory (padded by 16: ldmatrix rows hit distinct banks)
   int half, stage, off_pos, off_tab, off_bar, total;
-  __host__ __device__ DLayout(int Hkv, int D) {
+  __host__ __device__ DLayout(int Hkv, int D, int NS) {
     row = Hkv * D * 2 + 16;
     half = kKeys * row;
     stage = 2 * half;
-    off_pos = kStages * stage;                             // int [kStages][kKeys]
-    off_tab = (off_pos + kStages * kKeys * 4 + 15) & ~15;  // Entry [kTab]
-    off_bar = off_tab + kTab * static_cast<int>(sizeof(Entry));  // full[kStages], empty[kStages]
-    total = off_bar + 2 * kStages * 8;
+    off_pos = NS * stage;                             // int [NS][kKeys]
+    off_tab = (off_pos + NS * kKeys * 4 + 15) & ~15;  // Entry [kTab]
+    off_bar = off_tab + kTab * static_cast<int>(sizeof(Entry));  // full[NS], empty[NS]
+    total = off_bar + 2 * NS * 8;
   }
 };
 
@@ -200,15 +201,15 @@ __device__ __forceinline__ void finish_batch(const DraftParams& p, const RawEntr
 }
 
 // MAXW: the most KV heads (consumer warps) this instantiation serves; PACK: at most 8
-// query heads a KV head (their P high and low parts share one MMA).
-template <int D, int MAXW, bool PACK>
+// query heads a KV head (their P high and low parts share one MMA); NS: ring stages.
+template <int D, int MAXW, bool PACK, int NS>
 __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const DLayout L(p.Hkv, D);
+  const DLayout L(p.Hkv, D, NS);
   int* posb = reinterpret_cast<int*>(smem + L.off_pos);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.off_bar);
-  uint64_t* empty = full + kStages;
+  uint64_t* empty = full + NS;
   const int W = p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float NEG = neg_inf();
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   RawEntry r0{0, 0, 0, 0, 0};
   if (p.settled && mine) r0 = load_entry(p, e0, x1, S);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], W);
     }
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   // dependency wait): a slot of a chunk that loads no page keeps either these zeros or
   // a value row an earlier chunk attended, so 0 * V stays exact without zeroing rows on
   // the producer's critical path.
-  for (int st = 0; st < kStages; ++st) {
+  for (int st = 0; st < NS; ++st) {
     uint4* vr = reinterpret_cast<uint4*>(smem + st * L.stage + L.half);
     for (int i = threadIdx.x; i < L.half / 16; i += blockDim.x) vr[i] = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -291,11 +292,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     // With a settled selection the first chunks' selected pages (as many chunks as the
     // ring holds) are requested before the dependency wait; their draft-token pages (the
     // previous step appended the last of them) and every later chunk wait for it.
-    int ex[kStages], en[kStages];
+    int ex[NS], en[NS];
     int nearly = 0;
     if (p.settled) {
 #pragma unroll
-      for (int i = 0; i < kStages; ++i) {
+      for (int i = 0; i < NS; ++i) {
         if (x < x1) {
           const int nvalid = min(kKeys, min(x1 - x, S - j));
           issue_chunk(i, x, nvalid, 1);
@@ -320,16 +321,16 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     pdl_wait();
     pdl_launch_dependents();
 #pragma unroll
-    for (int i = 0; i < kStages; ++i)
+    for (int i = 0; i < NS; ++i)
       if (i < nearly) issue_chunk(i, ex[i], en[i], 2);
     issued = nearly;
-    stage = nearly % kStages;
-    phase = static_cast<uint32_t>((nearly / kStages) & 1);
+    stage = nearly % NS;
+    phase = static_cast<uint32_t>((nearly / NS) & 1);
     while (x < x1) {
       const int nvalid = min(kKeys, min(x1 - x, S - j));
       if (x + nvalid > res_end) advance_tables();
       bool ok_wait = true;
-      if (lane == 0 && issued >= kStages) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
+      if (lane == 0 && issued >= NS) ok_wait = mbar_wait(&empty[stage], phase ^ 1u, p.status);
       if (!__shfl_sync(0xffffffffu, ok_wait, 0)) break;
       issue_chunk(stage, x, nvalid, 0);
       ++issued;
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
         j = 0;
         ++b;
       }
-      if (++stage == kStages) {
+      if (++stage == NS) {
         stage = 0;
         phase ^= 1u;
       }
@@ -347,8 +348,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
     // no copy may still be in flight when the CTA exits, also when a consumer gave up
     // (normally the consumers have already seen every chunk land)
     if (lane == 0)
-      for (int c = issued > kStages ? issued - kStages : 0; c < issued; ++c)
-        mbar_wait(&full[c % kStages], static_cast<uint32_t>((c / kStages) & 1), p.status);
+      for (int c = issued > NS ? issued - NS : 0; c < issued; ++c)
+        mbar_wait(&full[c % NS], static_cast<uint32_t>((c / NS) & 1), p.status);
     __syncwarp();
     return;
   }
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
       softmax_pv16<D, PACK>(st, s, vaddr, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == kStages) {
+      if (++stage == NS) {
         stage = 0;
         phase ^= 1u;
       }
@@ -564,10 +565,10 @@ __global__ void __launch_bounds__(NW * 32) draft_combine_kernel(const DraftParam
   }
 }
 
-template <int D, int MAXW, bool PACK>
+template <int D, int MAXW, bool PACK, int NS>
 cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) {
-  const size_t smem = static_cast<size_t>(DLayout(p.Hkv, D).total) + 128;
-  cudaError_t e = ensure_smem<draft_kernel<D, MAXW, PACK>>(smem);
+  const size_t smem = draft_smem_bytes(D, p.Hkv, NS);
+  cudaError_t e = ensure_smem<draft_kernel<D, MAXW, PACK, NS>>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -579,7 +580,7 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
   cfg.stream = stream;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  if ((e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW, PACK>, p)) != cudaSuccess) return e;
+  if ((e = cudaLaunchKernelEx(&cfg, draft_kernel<D, MAXW, PACK, NS>, p)) != cudaSuccess) return e;
   const int nw = draft_combine_warps(p.B, p.slots, p.nctas);
   if (nw == 0) return cudaSuccess;  // every sequence was finished by the CTA holding it
   cudaLaunchConfig_t cfg2 = {};
@@ -595,7 +596,17 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
 
 }  // namespace
 
-size_t draft_smem_bytes(int D, int Hkv) { return static_cast<size_t>(DLayout(Hkv, D).total) + 128; }
+size_t draft_smem_bytes(int D, int Hkv, int nstage) {
+  return static_cast<size_t>(DLayout(Hkv, D, nstage).total) + 128;
+}
+
+// Three stages pay off when a CTA has several chunks to stream (more bytes in flight);
+// with one or two chunks a CTA the deeper ring only lengthens the set-up.
+int draft_stages(int D, int Hkv, int B, int slots, int nctas, size_t smem_optin) {
+  const int64_t per_cta = (static_cast<int64_t>(B) * slots + nctas - 1) / nctas;
+  if (per_cta >= 4 * kKeys && draft_smem_bytes(D, Hkv, kMaxStages) <= smem_optin) return kMaxStages;
+  return kMinStages;
+}
 
 int draft_combine_warps(int B, int slots, int nctas) {
   const int64_t E = static_cast<int64_t>(B) * slots;
@@ -611,14 +622,19 @@ int draft_combine_warps(int B, int slots, int nctas) {
 }
 
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl) {
-  const bool pack = p.G <= 8;
+  const bool pack = p.G <= 8, deep = p.nstage == 3;
+#define VG_DRAFT_FORMS(D_, W_)                                                          \
+  return pack ? (deep ? launch_draft_t<D_, W_, true, 3>(p, stream, pdl)                  \
+                      : launch_draft_t<D_, W_, true, 2>(p, stream, pdl))                 \
+              : (deep ? launch_draft_t<D_, W_, false, 3>(p, stream, pdl)                 \
+                      : launch_draft_t<D_, W_, false, 2>(p, stream, pdl))
   if (p.Hkv <= 8) {
-    if (p.D == 64) return pack ? launch_draft_t<64, 8, true>(p, stream, pdl) : launch_draft_t<64, 8, false>(p, stream, pdl);
-    if (p.D == 128)
-      return pack ? launch_draft_t<128, 8, true>(p, stream, pdl) : launch_draft_t<128, 8, false>(p, stream, pdl);
+    if (p.D == 64) VG_DRAFT_FORMS(64, 8);
+    if (p.D == 128) VG_DRAFT_FORMS(128, 8);
   } else if (p.D == 64) {  // (more than 8 KV heads at d = 128 exceed a 1024-element page)
-    return pack ? launch_draft_t<64, 16, true>(p, stream, pdl) : launch_draft_t<64, 16, false>(p, stream, pdl);
+    VG_DRAFT_FORMS(64, 16);
   }
+#undef VG_DRAFT_FORMS
   return cudaErrorInvalidValue;
 }
 

@@ -381,7 +381,7 @@ vg_status check_draft_page(const Shape& s) {
 // Pipeline stages of the draft kernel: two when they fit beside the run partials.
 vg_status check_draft_smem(const Shape& s, const DevInfo& di) {
   if (const vg_status st = check_draft_page(s); st != VG_OK) return st;
-  if (draft_smem_bytes(s.D, s.Hkv) > di.smem_optin)
+  if (draft_smem_bytes(s.D, s.Hkv, 2) > di.smem_optin)
     return fail(VG_ERR_UNSUPPORTED_SHAPE, "sparse draft: H_kv * d = %d needs more shared memory than a CTA has",
                 s.Hkv * s.D);
   return VG_OK;
@@ -417,6 +417,7 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.settled = a.settled ? 1 : 0;
   p.nctas = draft_ctas(di.sms);
+  p.nstage = draft_stages(s.D, s.Hkv, s.B, p.slots, p.nctas, di.smem_optin);
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);
   p.out = static_cast<__nv_bfloat16*>(a.out);

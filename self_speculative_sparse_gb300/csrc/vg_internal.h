@@ -86,6 +86,7 @@ struct DraftParams {
   int B, Hq, Hkv, G, D;
   float scale, scale_log2;
   int nctas;
+  int nstage;                  // ring stages of the draft kernel (2 or 3)
   float* part_o;               // [nctas + B][Hq][D]  unnormalised partial outputs
   float* part_ml;              // [nctas + B][Hq][2]
   __nv_bfloat16* out;          // [B][Hq][D]
@@ -123,7 +124,8 @@ size_t topk_smem_bytes(int per_cta);
 cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t* idx, int32_t* count,
                           int32_t* status, cudaStream_t stream);
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
-size_t draft_smem_bytes(int D, int Hkv);
+size_t draft_smem_bytes(int D, int Hkv, int nstage);  // dynamic shared memory of a draft CTA
+int draft_stages(int D, int Hkv, int B, int slots, int nctas, size_t smem_optin);  // 2 or 3
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 int accept_chunks(int V);  // vocabulary chunks of the statistics kernel
 // Warps of the draft step's combine kernel (4, 8 or 16 from the most partials a

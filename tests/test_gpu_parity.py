@@ -54,6 +54,14 @@ CASES = {
     # tolerance here (1.02 of it, against 0.32 with P's low part)
     "two_sinks_short": Workload("sinks2", B=24, Hq=16, Hkv=4, d=128, gamma=3, k=6, n=None, ragged=(2, 90),
                                 scheme="heavy", heavy_frac=0.02, sinks=2, u_per_seq=True, seed=85),
+    # at least 64 entries a draft CTA: the draft kernel's three-stage ring, in its
+    # packed (at most 8 query heads a KV head), unpacked and 16-warp forms
+    "deep_ring_d128": Workload("deep128", B=12, Hq=32, Hkv=8, d=128, gamma=3, k=1000, n=None, ragged=(1001, 1300),
+                               seed=88),
+    "deep_ring_g16": Workload("deep16", B=12, Hq=16, Hkv=1, d=128, gamma=3, k=1000, n=None, ragged=(1001, 1300),
+                              seed=89),
+    "deep_ring_hkv16_d64": Workload("deep64", B=12, Hq=32, Hkv=16, d=64, gamma=3, k=1000, n=None,
+                                    ragged=(1001, 1300), seed=90),
 }
 
 
