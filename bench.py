@@ -61,6 +61,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="only the first N layers of a multi-layer workload (small profiling captures)")
     return ap.parse_args(argv)
 
 
@@ -236,6 +238,22 @@ def profiled_traffic(kernel: str, workload: str, files) -> int | None:
         return int(float(vals["dram_bytes_per_launch"]))
     except (KeyError, ValueError):
         return None
+
+
+def roofline_parts(w, S, fr, peaks, verify_launches) -> dict:
+    """The three roofline fractions (verify call, fused verify + select, draft phase),
+    each with the per-launch DRAM traffic of its dominant kernel where a committed ncu
+    summary of the current sources has it (else null)."""
+    parts = {k: {"bound": "hbm", "achieved": v["achieved_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": v["frac"]} for k, v in fr.items()}
+    vt = profiled_traffic("verify_attn", w.name, VERIFY_SOURCES)
+    for k in ("verify_call", "verify_select"):
+        parts[k].update({"kernel": "verify_kernel", "traffic": vt,
+                         "algorithmic_bytes_per_launch": S.nbytes["verify"] / verify_launches})
+    parts["draft_phase"].update({"kernel": "draft_kernel",
+                                 "traffic": profiled_traffic("draft_attn", w.name, DRAFT_SOURCES),
+                                 "algorithmic_bytes_per_launch": S.nbytes["draft"] / (w.gamma * verify_launches)})
+    return parts
 
 
 def pack_views(state, names, copy_values: bool):
@@ -595,6 +613,8 @@ def run_ours(args, rank, local, world):
     torch.cuda.set_device(local)
     vbuild.build()
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = synth.scaled(w, layers=min(w.layers, args.layers))
     S = Setup(w, local)
     stream, multi, ncopy = S.stream, S.multi, S.ncopy
 
@@ -770,8 +790,7 @@ def run_ours(args, rank, local, world):
                      "traffic": profiled_traffic("verify_attn", w.name, VERIFY_SOURCES),
                      "algorithmic_bytes_per_launch": S.nbytes["verify"] / verify_launches,
                      "launch_us": ph["verify_call"] / verify_launches,
-                     "parts": {k: {"bound": "hbm", "achieved": v["achieved_gbs"], "peak": peaks["hbm_gbs"],
-                                   "unit": "GB/s", "frac": v["frac"]} for k, v in fr.items()}},
+                     "parts": roofline_parts(w, S, fr, peaks, verify_launches)},
         "e2e": {"value": e2e_s / e2e_steps * 1e6 / world, "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo,
                 "api": "vg_iteration_plan_launch (each buffer set's iteration captured once at set-up)",
