@@ -300,8 +300,12 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
     __syncwarp();
   } else if (PAGED && ntiles > 0 && warp == C::RWARPS) {
     // ---------------------------------------------------------------- TMA producer (paged)
-    // A tile of 64 keys is 64 / box_rows boxes, each at its page's physical rows; lane s
-    // issues boxes s and s + 32.  Boxes wholly past the prefix are not loaded (their rows
+    // A tile of 64 keys is WPT = 64 / box_rows boxes (page pieces; pages of 8, 16, 32
+    // tokens or a multiple of 64, so WPT <= 8), each at its page's physical rows; lane s
+    // issues box s.  The page-table words are loaded a batch ahead, one a lane (tile
+    // base + lane / WPT, box lane % WPT) with an unconditional, clamped load, and reach
+    // the issuing lanes by shuffle when their tile is issued: no load's latency sits
+    // between two tiles' copies.  Boxes wholly past the prefix are not loaded (their rows
     // are masked, and the row warps zero such value rows).  Lane 0 takes the waits and
     // the byte count.
     int b, g, j;
@@ -311,41 +315,33 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
       tma_prefetch_desc(&tmV);
     }
     const int BR = p.box_rows;
-    // Row of box s of tile (b, j) for the lane's two boxes (-1: no box), looked up one
-    // tile ahead so that the table's loads overlap the wait for the ring.
-    auto lookup = [&](int bb, int jj, int (&y)[2]) {
-      const int keys = min(TK, nlen[bb] - jj * TK);  // keys of the tile inside the prefix (> 0)
-      const int nbox = (keys + BR - 1) / BR;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int s_ = lane + 32 * k;
-        y[k] = -1;
-        if (s_ >= nbox) continue;
-        const int64_t slot =
-            kv_slot(p.seq_offset, p.ptab, p.psize, p.pstride, p.capacity, bb, static_cast<int64_t>(jj) * TK + s_ * BR);
-        if (slot < 0) report(p.status, VG_ERR_DEVICE_BOUNDS);
-        y[k] = static_cast<int>(slot);
-      }
+    const int WPT = TK / BR;   // page words a tile
+    const int TPB = 32 / WPT;  // tiles a batch of words
+    // word and kind (0: no box, 1: past the sequence's table, 2: a table word) of this
+    // lane's box in the batch starting at tile `base`
+    auto load_words = [&](int base, int& w, int& kind) {
+      const int ti = base + lane / WPT, sb = lane % WPT;
+      int bb = 0, gg = 0, jj = 0;
+      if (ti < ntiles) locate(t0 + ti, cum, p.B, p.Hkv, bb, gg, jj);
+      const int keys = ti < ntiles ? min(TK, nlen[bb] - jj * TK) : 0;
+      const int pos = jj * TK + sb * BR;
+      const int lim = p.pstride * p.psize;
+      kind = sb * BR >= keys ? 0 : (pos < lim ? 2 : 1);
+      const int pi = min(pos, lim - 1) / p.psize;  // (always inside the table: the load is unconditional)
+      w = p.ptab[static_cast<size_t>(bb) * p.pstride + pi];
     };
-    // rows of tiles i .. i + LA - 1 (a ring of lookups, LA tiles ahead of the copies)
-    constexpr int LA = 4;
-    int yq[LA][2];
-    int bl = b, gl = g, jl = j;  // the lookup cursor
-    for (int i = 0; i < LA && i < ntiles; ++i) {
-      lookup(bl, jl, yq[i]);
-      advance(bl, gl, jl, cum, p.B, p.Hkv);
-    }
-    int issued = 0;
+    int cw, ck, nw, nk;
+    load_words(0, cw, ck);
+    load_words(TPB, nw, nk);
+    int base = 0, issued = 0;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i % S;
-      int ycur[2] = {yq[i % LA][0], yq[i % LA][1]};
-      // the rows of tile i + LA, while this tile waits for its stage
-      if (i + LA < ntiles) {
-        lookup(bl, jl, yq[i % LA]);
-        advance(bl, gl, jl, cum, p.B, p.Hkv);
+      if (i - base == TPB) {  // the next batch (loaded a batch ago), and the one after it
+        cw = nw;
+        ck = nk;
+        base += TPB;
+        load_words(base + TPB, nw, nk);
       }
-      int bn = b, gn = g, jn = j;
-      advance(bn, gn, jn, cum, p.B, p.Hkv);
+      const int st = i % S;
       // after the first stage, the first run's query rows go first: issued together
       // with the whole ring, their loads would queue behind it (about 3 us at the start)
       bool ok = true;
@@ -354,29 +350,32 @@ __global__ void __launch_bounds__(TCfg<D, MR>::THREADS, 1)
         if (ok && i >= S) ok = mbar_wait_ab(&empty[st], ((i / S) - 1) & 1, p.status, abort);
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const int nload = __popc(__ballot_sync(0xffffffffu, ycur[0] >= 0)) + __popc(__ballot_sync(0xffffffffu, ycur[1] >= 0));
+      const int src = (i - base) * WPT + (lane < WPT ? lane : 0);
+      const int w = __shfl_sync(0xffffffffu, cw, src), kind = __shfl_sync(0xffffffffu, ck, src);
+      int y = -1;
+      if (lane < WPT && kind != 0) {
+        if (kind == 1 || w < 0 || (static_cast<int64_t>(w) + 1) * p.psize > p.capacity)
+          report(p.status, VG_ERR_DEVICE_BOUNDS);
+        else
+          y = w * p.psize + (j * TK + lane * BR) % p.psize;
+      }
+      const int nload = __popc(__ballot_sync(0xffffffffu, y >= 0));
       if (lane == 0) {
         fence_proxy_async_smem();  // the stage may hold zeros written by the generic proxy
         mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nload * BR * 128 * C::HALVES * 2));
       }
       __syncwarp();
-      uint8_t* kdst = smem + st * C::STAGE_BYTES;
-      uint8_t* vdst = kdst + C::TILE_BYTES;
+      if (y >= 0) {
+        uint8_t* kdst = smem + st * C::STAGE_BYTES + lane * BR * 128;
+        uint8_t* vdst = kdst + C::TILE_BYTES;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        if (ycur[k] >= 0) {
-          const int off = (lane + 32 * k) * BR * 128;
-#pragma unroll
-          for (int h = 0; h < C::HALVES; ++h) {
-            tma_load_2d(kdst + h * C::HALF_BYTES + off, &tmK, g * D + h * 64, ycur[k], &full[st]);
-            tma_load_2d(vdst + h * C::HALF_BYTES + off, &tmV, g * D + h * 64, ycur[k], &full[st]);
-          }
+        for (int h = 0; h < C::HALVES; ++h) {
+          tma_load_2d(kdst + h * C::HALF_BYTES, &tmK, g * D + h * 64, y, &full[st]);
+          tma_load_2d(vdst + h * C::HALF_BYTES, &tmV, g * D + h * 64, y, &full[st]);
         }
       }
       ++issued;
-      b = bn;
-      g = gn;
-      j = jn;
+      advance(b, g, j, cum, p.B, p.Hkv);
     }
     // no copy may still be in flight when the CTA exits (normally all were consumed)
     if (lane == 0)
