@@ -644,7 +644,9 @@ size_t vg_accept_workspace_size(int32_t B, int32_t gamma, int32_t V) {
     return 0;
   }
   const size_t rows = static_cast<size_t>(B) * (2 * gamma + 1);
-  return up256(rows * accept_chunks(V) * 16);
+  // per-chunk statistics, per-sequence decision records (32 B), per-tile sums
+  return up256(rows * accept_chunks(V) * 16) + up256(static_cast<size_t>(B) * 32) +
+         up256(static_cast<size_t>(B) * 2 * accept_tiles(V) * 4);
 }
 
 vg_status vg_accept(int32_t B, int32_t gamma, int32_t V, const float* p_logits, const float* q_logits,
@@ -677,7 +679,12 @@ vg_status vg_accept(int32_t B, int32_t gamma, int32_t V, const float* p_logits, 
   p.V = V;
   p.nchunk = accept_chunks(V);
   p.sample = sample ? 1 : 0;
+  const size_t rows = static_cast<size_t>(B) * (2 * gamma + 1);
+  const size_t off_dec = up256(rows * accept_chunks(V) * 16);
   p.stats = static_cast<float*>(ws);
+  p.dec = reinterpret_cast<float*>(static_cast<char*>(ws) + off_dec);
+  p.tiles = reinterpret_cast<float*>(static_cast<char*>(ws) + off_dec + up256(static_cast<size_t>(B) * 32));
+  p.ntiles = accept_tiles(V);
   p.n_accept = n_accept;
   p.next_token = next_token;
   p.advance_len = advance_len;

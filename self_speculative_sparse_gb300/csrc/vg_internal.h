@@ -104,6 +104,9 @@ struct AcceptParams {
   const float* u_res;      // [B] (sampling only)
   int B, gamma, V, nchunk, sample;
   float* stats;            // [rows][nchunk] (max, sum, argmax value, argmax) per chunk
+  float* dec;              // [B] decision records (sampling): a, row a's statistics
+  float* tiles;            // [B][2][ntiles] tile sums of row a's weights: excess, then p
+  int ntiles;
   int32_t* n_accept;       // [B]
   int32_t* next_token;     // [B]
   int32_t* advance_len;    // [B] or null
@@ -128,6 +131,7 @@ size_t draft_smem_bytes(int D, int Hkv, int nstage);  // dynamic shared memory o
 int draft_stages(int D, int Hkv, int B, int slots, int nctas, size_t smem_optin);  // 2 or 3
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 int accept_chunks(int V);  // vocabulary chunks of the statistics kernel
+int accept_tiles(int V);   // tiles of the sampling draw over a row of V entries
 // Warps of the draft step's combine kernel (4, 8 or 16 from the most partials a
 // sequence has), or 0 when every sequence's entries sit in one CTA (no combine runs).
 int draft_combine_warps(int B, int slots, int nctas);
