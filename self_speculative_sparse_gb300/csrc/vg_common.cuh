@@ -251,29 +251,6 @@ __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sy
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-// ------------------------------------------------------------------ thread-block clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-// Split cluster barrier: every thread of every CTA of the cluster arrives once per
-// phase (release: its earlier writes, shared memory included, become visible to the
-// cluster) and waits before touching what the others wrote (acquire).
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// Generic address of the same shared-memory location in CTA `rank` of the cluster.
-template <typename T>
-__device__ __forceinline__ const T* map_rank(const T* p, uint32_t rank) {
-  uint64_t out;
-  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
-  return reinterpret_cast<const T*>(out);
-}
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue now / wait until the previous kernel's results are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {
