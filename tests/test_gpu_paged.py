@@ -2,8 +2,9 @@
 as a paged attention whose pages are tokens).
 
 The same layers are laid out in pages scattered over the pool by a seeded permutation:
-* a whole iteration (verify, selection, draft steps) with pages of 8, 16 and 64 tokens
-  matches the oracle, including the appends landing in the right physical slots;
+* a whole iteration (verify, selection, draft steps) with pages of 8, 16, 32, 64 and 128
+  tokens matches the oracle, including the appends landing in the right physical slots,
+  also with prefixes long enough that each verify CTA streams tens of tiles;
 * it matches the slot-pool layout of the same data bit for bit (the layout changes the
   addressing, not the arithmetic);
 * the draft step alone reads pages of one token (the page indices are token slots);
@@ -38,14 +39,30 @@ CASES = {
     "ragged_b6": scaled(W["loop32"], B=6, layers=1, ragged=(1, 1500)),
     "batched_b3_n700": scaled(W["batched"], B=3, n=700),
     "g16_m64_d64": Workload("g16d64", B=2, Hq=16, Hkv=1, d=64, gamma=3, k=100, n=777, seed=84),
+    # at least 64 entries a draft CTA: the draft kernel's three-stage ring through pages
+    "deep_ring_d128": Workload("deep128", B=12, Hq=32, Hkv=8, d=128, gamma=3, k=1000, n=None, ragged=(1001, 1300),
+                               seed=88),
 }
 
 
-@pytest.mark.parametrize("P", [8, 16, 64])
+@pytest.mark.parametrize("P", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("name", list(CASES))
 def test_paged_iteration_matches_oracle_and_the_slot_pool(name, P):
+    _paged_matches(CASES[name], P)
+
+
+# Long prefixes: each verify CTA streams some 60-70 tiles, so its producer goes through
+# several batches of page-table words (32 tiles a batch at 64-token pages, 8 at 16).
+LONG = Workload("paged_long", B=4, Hq=32, Hkv=8, d=128, gamma=6, k=512, n=None, ragged=(15000, 22000), seed=91)
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_paged_long_prefixes_match_oracle_and_the_slot_pool(P):
+    _paged_matches(LONG, P)
+
+
+def _paged_matches(w, P):
     from self_speculative_sparse_gb300.runtime import LayerState
-    w = CASES[name]
     flat = w.layer_pool(0)
     paged = synth.to_paged(w, flat, P, seed=P)
     a = LayerState(w, flat)
