@@ -62,6 +62,11 @@ CASES = {
                               seed=89),
     "deep_ring_hkv16_d64": Workload("deep64", B=12, Hq=32, Hkv=16, d=64, gamma=3, k=1000, n=None,
                                     ragged=(1001, 1300), seed=90),
+    # more sequences than draft CTAs, each a few entries: a CTA holds whole sequences and
+    # finishes them itself (bf16 output and the token's append in the draft kernel)
+    "complete_in_cta": Workload("b304", B=304, Hq=8, Hkv=2, d=64, gamma=3, k=8, n=None, ragged=(9, 60), seed=92),
+    # ... and with a split that leaves some sequences whole in a CTA and cuts others
+    "mixed_complete": Workload("b200", B=200, Hq=8, Hkv=2, d=64, gamma=3, k=8, n=None, ragged=(9, 60), seed=93),
 }
 
 
@@ -367,3 +372,42 @@ def test_window_selection_matches_oracle():
             assert np.array_equal(gi[b, :len(want)], want), (k, b)
             assert (gi[b, len(want):] == -1).all(), (k, b)
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("name", ["llama8b_n1000", "ragged_b6", "deep_ring_d128", "complete_in_cta"])
+def test_settled_draft_steps_equal_plain_ones(name):
+    """VG_DRAFT_SELECTION_SETTLED only moves the gather of the selected entries ahead of
+    the dependency wait: the steps' outputs and appends are bit-identical to those of
+    calls without the flag (and those match the oracle through the iteration tests)."""
+    from self_speculative_sparse_gb300.runtime import LayerState
+    w = CASES[name]
+    pool = w.layer_pool(0)
+    tl = [torch.full((w.B,), s + 1, dtype=torch.int32, device="cuda") for s in range(w.gamma)]
+    outs = []
+    for settled in (False, True):
+        st = LayerState(w, pool)
+        st.verify()
+        st.select()
+        for s in range(w.gamma):
+            st.draft_step(s, tl[s], settled=settled and s > 0)
+        torch.cuda.synchronize()
+        assert st.check_status() == 0
+        outs.append((st.out_draft.view(torch.int16).clone(), st.K.view(torch.int16).clone(),
+                     st.V.view(torch.int16).clone()))
+    for x, y, nm in zip(outs[0], outs[1], ("draft outputs", "K cache", "V cache")):
+        assert torch.equal(x, y), nm
+
+
+def test_draft_launch_count():
+    """vg_sparse_draft_launches: 1 when each sequence's entries fall to a single CTA of the
+    step's grid (that CTA finishes it), else 2 (a second kernel merges the partials)."""
+    from self_speculative_sparse_gb300 import binding as vb
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ctas = min(sms, 512)
+    dims = lambda B: vb.make_dims(B=B, H_q=8, H_kv=2, d=64, gamma=3, max_len=4096)
+    # one sequence of 2048 + 4 entries over every CTA: merged by a second kernel
+    assert vb.vg_sparse_draft_launches(dims(1), 2048, 4) == 2
+    # as many sequences as CTAs, 4 + 4 entries each: one CTA a sequence
+    assert vb.vg_sparse_draft_launches(dims(ctas), 4, 4) == 1
+    # a device tail array bounds the tail at 16: still whole sequences a CTA
+    assert vb.vg_sparse_draft_launches(dims(ctas), 4, 0) == 1
