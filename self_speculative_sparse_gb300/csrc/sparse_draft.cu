@@ -14,11 +14,14 @@
 //     the split needs no device data and each CTA's first round trip fetches its
 //     positions.
 //   * Every thread resolves one of the CTA's first entries (position, cache slot) into
-//     a shared-memory table during the set-up; the producer warp resolves later
-//     entries a batch ahead, so no position round trip sits on the per-chunk path.
-//   * A producer warp turns each entry into two bulk copies of a whole page (large
-//     requests keep the copy engine efficient; the current draft token comes straight
-//     from the inputs) into a padded shared-memory ring guarded by mbarriers; one
+//     a shared-memory table during the set-up; each producer warp resolves later
+//     entries a batch ahead into its own ring, so no position round trip sits on the
+//     per-chunk path.
+//   * Two producer warps turn each entry into a bulk copy of a whole page each, one the
+//     key page, the other the value page (large requests keep the copy engine
+//     efficient, and a warp issues copies at a bounded rate; the current draft token
+//     comes straight from the inputs) into a padded shared-memory ring guarded by
+//     mbarriers; one
 //     consumer warp per KV head runs Q K^T and P V on bf16 tensor cores with fp32
 //     online softmax, P carried as a bf16 high and low part.
 //   * Within a draft phase the selection does not change between steps.  When the
@@ -68,8 +71,8 @@ struct DLayout {
     half = kKeys * row;
     stage = 2 * half;
     off_pos = NS * stage;                             // int [NS][kKeys]
-    off_tab = (off_pos + NS * kKeys * 4 + 15) & ~15;  // Entry [kTab]
-    off_bar = off_tab + kTab * static_cast<int>(sizeof(Entry));  // full[NS], empty[NS]
+    off_tab = (off_pos + NS * kKeys * 4 + 15) & ~15;  // Entry [2][kTab]: each producer warp's own ring
+    off_bar = off_tab + 2 * kTab * static_cast<int>(sizeof(Entry));  // full[NS], empty[NS]
     total = off_bar + 2 * NS * 8;
   }
 };
@@ -203,7 +206,7 @@ __device__ __forceinline__ void finish_batch(const DraftParams& p, const RawEntr
 // MAXW: the most KV heads (consumer warps) this instantiation serves; PACK: at most 8
 // query heads a KV head (their P high and low parts share one MMA); NS: ring stages.
 template <int D, int MAXW, bool PACK, int NS>
-__global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftParams p) {
+__global__ void __launch_bounds__((MAXW + 2) * 32, 1) draft_kernel(const DraftParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const DLayout L(p.Hkv, D, NS);
@@ -253,25 +256,36 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
   if (x0 >= x1) return;
   const int page = p.Hkv * D * 2;  // bytes of one token's K (or V), all heads
 
-  // ------------------------------------------------------------------ producer warp
-  if (warp == W) {
+  // ------------------------------------------------------------------ producer warps
+  // Warp W issues the key pages (and keeps the positions and the byte counts), warp W + 1
+  // the value pages: a warp issues bulk copies at a bounded rate, and two halve the time
+  // to start a chunk's copies.  The two walk the same chunks and wait on the same
+  // barriers, each from its own ring of resolved entries (no exchange between them).
+  if (warp >= W) {
+    const int role = warp - W;  // 0: keys, 1: values
+    Entry* ring = tab + role * kTab;
+    if (role == 1) {  // the set-up's entries, into this warp's own ring
+      for (int i = lane; i < n0; i += 32) ring[i] = tab[i];
+      __syncwarp();
+    }
     // Later entries are resolved a batch ahead: a batch's table entries are written
     // when the chunks reach it, while the next batch's loads are already in flight.
     RawEntry raw[kBatch / 32];
-    int res_end = min(x1, x0 + n0);  // entries [x0, res_end) are in the table
+    int res_end = min(x1, x0 + n0);  // entries [x0, res_end) are in the ring
     if (res_end < x1) load_batch(p, raw, res_end, x1, S, lane);
     auto advance_tables = [&]() {
-      finish_batch<D>(p, raw, tab, x0, res_end, x1, S, lane);
+      finish_batch<D>(p, raw, ring, x0, res_end, x1, S, lane);
       res_end = min(x1, res_end + kBatch);
       if (res_end < x1) load_batch(p, raw, res_end, x1, S, lane);
       __syncwarp();
     };
-    // Chunk [x, x + nvalid) into stage st: its positions for the consumers, the byte
-    // count on the stage's barrier and the copies.  part: 0 all pages, 1 all but the
-    // draft-token slots, 2 only those (for a chunk whose part 1 is already issued).
+    // Chunk [x, x + nvalid) into stage st: (keys) its positions for the consumers and
+    // the byte count on the stage's barrier, and this warp's copies.  part: 0 all
+    // pages, 1 all but the draft-token slots, 2 only those (a chunk whose part 1 is
+    // already issued).
     auto issue_chunk = [&](int st, int x, int nvalid, int part) {
-      const Entry t = lane < nvalid ? tab[(x + lane - x0) & (kTab - 1)] : Entry{nullptr, nullptr, -1, 0};
-      if (part != 2) {
+      const Entry t = lane < nvalid ? ring[(x + lane - x0) & (kTab - 1)] : Entry{nullptr, nullptr, -1, 0};
+      if (role == 0 && part != 2) {
         if (lane < kKeys) posb[st * kKeys + lane] = t.pos;
         const int nload = __popc(__ballot_sync(0xffffffffu, t.pos >= 0));
         __syncwarp();
@@ -280,8 +294,10 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) draft_kernel(const DraftPa
       }
       if (t.pos >= 0 && (part == 0 || (part == 1) == !t.tail)) {
         uint8_t* kst = smem + st * L.stage;
-        bulk_load(kst + lane * L.row, t.k, page, &full[st]);
-        bulk_load(kst + L.half + lane * L.row, t.v, page, &full[st]);
+        if (role == 0)
+          bulk_load(kst + lane * L.row, t.k, page, &full[st]);
+        else
+          bulk_load(kst + L.half + lane * L.row, t.v, page, &full[st]);
       }
     };
     int b = x0 / S, j = x0 - b * S;
@@ -575,7 +591,7 @@ cudaError_t launch_draft_t(const DraftParams& p, cudaStream_t stream, bool pdl) 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nctas);
-  cfg.blockDim = dim3((p.Hkv + 1) * 32);
+  cfg.blockDim = dim3((p.Hkv + 2) * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = at;
