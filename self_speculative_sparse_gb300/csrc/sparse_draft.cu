@@ -10,9 +10,9 @@
 //     and as many of V.  Each sequence's attended entries are its selected positions
 //     followed by the tail of draft-token slots.  The work is the fixed list of
 //     (sequence, entry slot) items - k_stride + a tail bound per sequence, slots past
-//     the sequence's entries masked - split evenly over one persistent CTA per SM, so
-//     the split needs no device data and each CTA's first round trip fetches its
-//     positions.
+//     the sequence's entries masked - split evenly over the step's CTAs (one a SM for a
+//     large step; fewer, of at least two chunks, for a small one), so the split needs no
+//     device data and each CTA's first round trip fetches its positions.
 //   * Every thread resolves one of the CTA's first entries (position, cache slot) into
 //     a shared-memory table during the set-up; each producer warp resolves later
 //     entries a batch ahead into its own ring, so no position round trip sits on the
@@ -45,7 +45,7 @@
 namespace vg {
 namespace {
 
-constexpr int kKeys = 16;  // entries per pipeline stage (one MMA key block)
+constexpr int kKeys = kDraftChunk;  // entries per pipeline stage (one MMA key block)
 constexpr int kMinStages = 2;  // ring stages: 2, or 3 for CTAs with many chunks (the host picks)
 constexpr int kMaxStages = 3;
 constexpr int kCombineRows = 12;  // partial rows a combine warp loads in one round
@@ -616,12 +616,30 @@ size_t draft_smem_bytes(int D, int Hkv, int nstage) {
   return static_cast<size_t>(DLayout(Hkv, D, nstage).total) + 128;
 }
 
-// Three stages pay off when a CTA has several chunks to stream (more bytes in flight);
+// Three stages pay off when a CTA has three chunks or more to stream (more bytes in
+// flight, and with a settled selection all three requested before the dependency wait);
 // with one or two chunks a CTA the deeper ring only lengthens the set-up.
 int draft_stages(int D, int Hkv, int B, int slots, int nctas, size_t smem_optin) {
   const int64_t per_cta = (static_cast<int64_t>(B) * slots + nctas - 1) / nctas;
-  if (per_cta >= 4 * kKeys && draft_smem_bytes(D, Hkv, kMaxStages) <= smem_optin) return kMaxStages;
+  if (per_cta > 2 * kKeys && draft_smem_bytes(D, Hkv, kMaxStages) <= smem_optin) return kMaxStages;
   return kMinStages;
+}
+
+// CTAs of a draft step.  A step with at least three chunks for every SM streams at the
+// HBM rate and takes every SM (each one's copies in flight count).  A smaller step is
+// bound by latency: it takes about 60% of the SMs, with at least two chunks a CTA, so
+// that the next step's CTAs start their set-up and early gather on the SMs this one
+// leaves free, and the merge has fewer partials.  (Measured on one-sequence steps of
+// 2055 and 4112 entries: 6.7 -> 5.3 us and 8.1 -> 6.8 us against one CTA per SM.)
+int draft_grid(int B, int slots, int sms) {
+  const int all = sms < 512 ? sms : 512;
+  const int64_t e = static_cast<int64_t>(B) * slots;
+  if (e >= static_cast<int64_t>(3) * kKeys * all) return all;
+  int64_t per = (e * 5 + 3 * all - 1) / (3 * all);  // e / (0.6 all), rounded up
+  if (per < 2 * kKeys) per = 2 * kKeys;
+  per = (per + kKeys - 1) / kKeys * kKeys;  // whole chunks
+  const int64_t n = (e + per - 1) / per;
+  return n < 1 ? 1 : (n > all ? all : static_cast<int>(n));
 }
 
 int draft_combine_warps(int B, int slots, int nctas) {

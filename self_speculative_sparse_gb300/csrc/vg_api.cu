@@ -176,8 +176,8 @@ vg_status check_mask(uint32_t mask, int R, const char* name) {
 // ---------------------------------------------------------------- workspace
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// CTAs of a draft step: one per SM (the combine gathers a sequence's partials in one
-// round with up to 16 warps of 12 rows each, and in later rounds beyond that).
+// Most CTAs of a draft step (one per SM, up to 512): sizes the draft partials of the
+// workspace (draft_grid picks the step's grid, at most this many).
 inline int draft_ctas(int sms) { return sms < 512 ? sms : 512; }
 
 struct WsLayout {
@@ -416,7 +416,7 @@ vg_status run_draft(const Shape& s, const vg_kv_cache* c, const DraftArgs& a, vo
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.settled = a.settled ? 1 : 0;
-  p.nctas = draft_ctas(di.sms);
+  p.nctas = draft_grid(s.B, p.slots, di.sms);
   p.nstage = draft_stages(s.D, s.Hkv, s.B, p.slots, p.nctas, di.smem_optin);
   p.part_o = at<float>(ws, w.dpart_o);
   p.part_ml = at<float>(ws, w.dpart_ml);
@@ -589,7 +589,7 @@ int32_t vg_sparse_draft_launches(const vg_dims* dims, int32_t k_stride, int32_t 
   if (device_info(&di) != VG_OK) return 0;
   if (check_draft_smem(s, di) != VG_OK) return 0;
   const int slots = k_stride + (tail_len_max ? tail_len_max : kDraftMaxTail);
-  return draft_combine_warps(s.B, slots, draft_ctas(di.sms)) > 0 ? 2 : 1;
+  return draft_combine_warps(s.B, slots, draft_grid(s.B, slots, di.sms)) > 0 ? 2 : 1;
 }
 
 size_t vg_workspace_size(const vg_dims* dims, int32_t k) {

@@ -15,6 +15,7 @@ constexpr int kVerifyTileKeys = 64;
 // Longest draft-token tail a sparse draft step attends besides the selection (the
 // draft tokens of one iteration number at most gamma + 1 <= 16).
 constexpr int kDraftMaxTail = 16;
+constexpr int kDraftChunk = 16;   // entries of one pipeline stage of the draft kernel
 // Most CTAs in one thread-block cluster of the draft step.
 constexpr int kDraftMaxCluster = 16;
 // Largest sequence the top-k kernel holds (in shared memory, across a cluster of up to 16).
@@ -129,6 +130,7 @@ cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t
 cudaError_t launch_draft(const DraftParams& p, cudaStream_t stream, bool pdl);
 size_t draft_smem_bytes(int D, int Hkv, int nstage);  // dynamic shared memory of a draft CTA
 int draft_stages(int D, int Hkv, int B, int slots, int nctas, size_t smem_optin);  // 2 or 3
+int draft_grid(int B, int slots, int sms);  // CTAs of a draft step
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t stream);
 int accept_chunks(int V);  // vocabulary chunks of the statistics kernel
 int accept_tiles(int V);   // tiles of the sampling draw over a row of V entries
