@@ -26,7 +26,7 @@
 //     online softmax, P carried as a bf16 high and low part.
 //   * Within a draft phase the selection does not change between steps.  When the
 //     caller says so (VG_DRAFT_SELECTION_SETTLED), the CTA resolves its first entries
-//     and the producer starts their page copies before the dependency wait, so the
+//     and the producer warps start their page copies before the dependency wait, so the
 //     gather overlaps the end of the previous step; only the draft-token tail, which
 //     the previous step appended, waits for it.  The draft kernel releases its
 //     dependents only after its own dependency wait, the combine at entry (its set-up
@@ -50,7 +50,7 @@ constexpr int kMinStages = 2;  // ring stages: 2, or 3 for CTAs with many chunks
 constexpr int kMaxStages = 3;
 constexpr int kCombineRows = 12;  // partial rows a combine warp loads in one round
 
-constexpr int kBatch = 128;  // entries the producer resolves in one round of loads (4 a lane)
+constexpr int kBatch = 128;  // entries a producer warp resolves in one round of loads (4 a lane)
 constexpr int kTab = 256;    // ring of resolved entries (two batches)
 
 // One resolved entry: its position (-1: masked), whether it is a draft-token slot
@@ -178,7 +178,7 @@ __device__ __forceinline__ Entry finish_entry(const DraftParams& p, const RawEnt
   return t;
 }
 
-// A batch of kBatch entries for the producer warp: entry xb + lane + 32 i.
+// A batch of kBatch entries for a producer warp: entry xb + lane + 32 i.
 __device__ __forceinline__ void load_batch(const DraftParams& p, RawEntry (&r)[kBatch / 32], int xb, int x1, int S,
                                            int lane) {
 #pragma unroll
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__((MAXW + 2) * 32, 1) draft_kernel(const DraftPa
   // The value rows of every stage start zeroed (shared memory only, so before the
   // dependency wait): a slot of a chunk that loads no page keeps either these zeros or
   // a value row an earlier chunk attended, so 0 * V stays exact without zeroing rows on
-  // the producer's critical path.
+  // the producers' critical path.
   for (int st = 0; st < NS; ++st) {
     uint4* vr = reinterpret_cast<uint4*>(smem + st * L.stage + L.half);
     for (int i = threadIdx.x; i < L.half / 16; i += blockDim.x) vr[i] = make_uint4(0u, 0u, 0u, 0u);
