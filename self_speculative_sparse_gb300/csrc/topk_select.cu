@@ -16,7 +16,11 @@
 // cluster through distributed shared memory (stores before the cluster barrier, so
 // that after it every CTA sums the cluster's counts from its own shared memory with
 // no remote round trip), and a scan over the digits by the 256 digit threads lets
-// every CTA pick the same digit.  A final cluster-wide exclusive scan in position order (the CTAs'
+// every CTA pick the same digit.  After two passes the keys still matching the 16-bit
+// prefix are usually few; each CTA then pushes its own into every CTA, and after one
+// cluster barrier every CTA finds the threshold among them itself instead of running
+// the last two passes (too many of them, as with many equal scores, and the passes run).
+// A final cluster-wide exclusive scan in position order (the CTAs'
 // counts pushed the same way) writes the selected positions, taking the needed
 // number of threshold-equal keys from the lowest positions.
 // Everything is integer work: the result is bit-exact and deterministic.
@@ -37,6 +41,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 256;  // radix digit: 8 bits
 constexpr int kListPerWarp = 256;  // candidate-list capacity of a warp for the last two passes
 constexpr int kMaxCluster = 16;    // CTAs per sequence (more than 8 needs the non-portable cluster size)
+// After two passes the keys still matching the 16-bit prefix are usually few: when no
+// CTA holds more than kCandPerCta of them and the cluster holds at most kThreads, every
+// CTA receives them all and finds the threshold among them itself, in place of the last
+// two passes (one cluster barrier instead of two, and no histograms).  Slices long
+// enough for the warps' candidate lists keep the two list passes, which cost less there.
+constexpr int kCandPerCta = 64;
 
 // fp32 -> key with the same order; -0.0 is mapped to the key of +0.0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -58,6 +68,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   // per-warp lists of the keys still in the running after two passes (passes 3 and 4
   // scan only these; a warp with more candidates than its list holds scans its keys)
   uint32_t* clist = reinterpret_cast<uint32_t*>(misc + 48);  // [kWarps][kListPerWarp]
+  uint32_t* cown = clist + kWarps * kListPerWarp;     // [kCandPerCta] this CTA's candidates
+  int* ccnt = reinterpret_cast<int*>(cown + kCandPerCta);  // [kMaxCluster] candidates of each CTA, pushed
+  uint32_t* cpush = reinterpret_cast<uint32_t*>(ccnt + kMaxCluster);  // [kMaxCluster][kCandPerCta], pushed
 
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
@@ -244,6 +257,63 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       }
       __syncwarp();
     }
+    if (pass == 1 && !lists) {  // the keys matching the 16-bit prefix, to every CTA (see kCandPerCta)
+      int* nloc = misc + 4;
+      if (tid == 0) {
+        *nloc = 0;
+        misc[6] = -1;  // (set below by the thread holding the threshold)
+      }
+      __syncthreads();
+      for (int i = tid; i < mine; i += kThreads) {
+        const uint32_t key = keys[i];
+        if ((key & pmask) == prefix) {
+          const int slot = atomicAdd(nloc, 1);  // (any order: only the multiset matters)
+          if (slot < kCandPerCta) cown[slot] = key;
+        }
+      }
+      __syncthreads();
+      const int nc = *nloc;
+      for (int e = tid; e < C * (kCandPerCta + 1); e += kThreads) {
+        const int rr = e / (kCandPerCta + 1), q = e - rr * (kCandPerCta + 1);
+        if (q == kCandPerCta)
+          *cluster.map_shared_rank(ccnt + r, rr) = nc;
+        else if (q < nc && nc <= kCandPerCta)
+          *cluster.map_shared_rank(cpush + r * kCandPerCta + q, rr) = cown[q];
+      }
+      cluster.sync();  // (these buffers are written once a launch)
+      int total = 0;
+      bool fits = true;
+      for (int rr = 0; rr < C; ++rr) {
+        total += ccnt[rr];
+        fits = fits && ccnt[rr] <= kCandPerCta;
+      }
+      if (fits && total <= kThreads) {
+        // the remaining-th largest candidate: thread t takes candidate t and counts the
+        // candidates above it and equal to it (the same decision in every CTA)
+        if (tid < total) {
+          int rr = 0, q = tid;
+          while (q >= ccnt[rr]) q -= ccnt[rr++];
+          const uint32_t x = cpush[rr * kCandPerCta + q];
+          int above = 0, same = 0;
+          for (int r2 = 0; r2 < C; ++r2)
+            for (int q2 = 0; q2 < ccnt[r2]; ++q2) {
+              const uint32_t y = cpush[r2 * kCandPerCta + q2];
+              above += y > x;
+              same += y == x;
+            }
+          if (above < remaining && remaining <= above + same) {  // (threads holding equal keys agree)
+            misc[5] = static_cast<int>(x);
+            misc[6] = remaining - above;
+          }
+        }
+        __syncthreads();
+        if (misc[6] > 0) {  // (always, for consistent counts; otherwise the last two passes run)
+          prefix = static_cast<uint32_t>(misc[5]);
+          remaining = misc[6];
+          break;
+        }
+      }
+    }
   }
   const uint32_t thr = prefix;  // k-th largest key; `remaining` keys equal to it are taken
 
@@ -362,7 +432,8 @@ cudaError_t launch_window(const int32_t* len, int B, int max_len, int k, int32_t
 
 size_t topk_smem_bytes(int per_cta) {
   return static_cast<size_t>(per_cta) * 4 + static_cast<size_t>(kWarps + 2 * kMaxCluster) * kBins * 4 +
-         (2 * kMaxCluster + 32 + 48) * 4 + static_cast<size_t>(kWarps) * kListPerWarp * 4;
+         (2 * kMaxCluster + 32 + 48) * 4 + static_cast<size_t>(kWarps) * kListPerWarp * 4 +
+         static_cast<size_t>(kCandPerCta + kMaxCluster + kMaxCluster * kCandPerCta) * 4;
 }
 
 cudaError_t launch_topk(const TopkParams& p, int cluster, cudaStream_t stream, bool pdl) {

@@ -214,7 +214,7 @@ def test_verify_reads_new_rows_from_cache_when_not_given():
 def test_topk_ties_signed_zero_and_edges():
     from self_speculative_sparse_gb300 import binding as vb
     rng = np.random.default_rng(3)
-    lens = [0, 1, 5, 1000, 40000, 70000]
+    lens = [0, 1, 5, 1000, 40000, 70000, 50000]
     B, L = len(lens), max(lens)
     sc = np.zeros((B, L), dtype=np.float32)
     for b, n in enumerate(lens):
@@ -222,6 +222,8 @@ def test_topk_ties_signed_zero_and_edges():
         v[v == 0] = np.where(rng.random((v == 0).sum()) < 0.5, -0.0, 0.0)
         if b == 4:
             v = rng.standard_normal(n).astype(np.float32) * 1e3     # spread values
+        if b == 6:  # a few equal scores in each 16-bit key class: the candidates exchanged
+            v = np.round(rng.standard_normal(n) * 1e3).astype(np.float32)   # after two passes tie
         sc[b, :n] = v
     dev = torch.from_numpy(sc).cuda()
     lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
